@@ -169,6 +169,23 @@ def oracle_prefill_sample(q, k, v, target_s: float, seed: int):
                                "cores": oracle.num_threads(lib)}
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor(values, dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def aggregate_value(flops_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job TFLOP/s: every rank does the same work; time is the slowest rank's."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
@@ -274,10 +291,7 @@ def run_ours(args, rank, world, local_rank):
     ms_pre = statistics.mean(t_pre)
     ms_dec = statistics.mean(t_dec)
     ms_e2e = statistics.mean(t_e2e)
-    vals = torch.tensor([ms_pre, ms_dec, ms_e2e, wall], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
-    ms_pre, ms_dec, ms_e2e, wall = [float(x) for x in vals.cpu()]
+    ms_pre, ms_dec, ms_e2e, wall = max_over_ranks([ms_pre, ms_dec, ms_e2e, wall], dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -299,7 +313,7 @@ def report_ours(args, res, world):
     peaks, src = load_peaks()
     flops = PREFILL.flops()
     tf_rank = flops / (res["ms_pre"] * 1e-3) / 1e12
-    value = tf_rank * world
+    value = aggregate_value(flops, res["ms_pre"], world)
     frac = tf_rank / peaks["bf16_tflops"]
     dec_bytes = res["kv_bytes"] + res["dec_other_bytes"]
     gbs = dec_bytes / (res["ms_dec"] * 1e-3) / 1e9
