@@ -88,14 +88,31 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check_bf16(name, t, ndim, device):
+def _check_tensor(name, t, dtype, shape, device):
+    """Metadata checks only (no device access): type, dtype, exact shape, layout, device."""
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.bfloat16 or t.dim() != ndim or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous {ndim}-d bfloat16 tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
     if t.device != device:
-        raise ValueError(f"{name} must be on {device}")
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def _check_bf16(name, t, ndim, device):
+    import torch
+    if isinstance(t, torch.Tensor) and t.dim() != ndim:
+        raise ValueError(f"{name} must be a {ndim}-d tensor")
+    _check_tensor(name, t, torch.bfloat16, None, device)
+
+
+def _require_cuda(device):
+    if device.type != "cuda":
+        raise ValueError(f"tensors must be CUDA tensors, got {device}")
 
 
 def attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None,
@@ -103,10 +120,12 @@ def attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None,
     """Fused attention forward through the C ABI.
 
     q [B,Hq,T,D], k/v [B,Hkv,T,D] bf16 CUDA tensors -> (o [B,Hq,T,D] bf16,
-    lse [B,Hq,T] fp32 or None).  ``scale`` defaults to 1/sqrt(D).
+    lse [B,Hq,T] fp32 or None).  ``scale`` defaults to 1/sqrt(D).  ``out`` and
+    ``lse``, when given, must be contiguous tensors of exactly those shapes and
+    dtypes on q's device.
     """
     import torch
-    device = q.device
+    device = q.device if isinstance(q, torch.Tensor) else None
     _check_bf16("q", q, 4, device)
     _check_bf16("k", k, 4, device)
     _check_bf16("v", v, 4, device)
@@ -114,17 +133,21 @@ def attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None,
     if k.shape[0] != B or k.shape[2] != T or k.shape[3] != D or v.shape != k.shape:
         raise ValueError("k/v must be [B, Hkv, T, D] matching q")
     Hkv = k.shape[1]
+    if out is not None:
+        _check_tensor("out", out, torch.bfloat16, (B, Hq, T, D), device)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, (B, Hq, T), device)
+    _require_cuda(device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    if out is None:
-        out = torch.empty_like(q)
-    else:
-        _check_bf16("out", out, 4, device)
-    if return_lse and lse is None:
-        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=device)
-    st = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                        lse.data_ptr() if lse is not None else None, B, Hq, Hkv, T, D,
-                        int(bool(causal)), float(scale), _stream_handle(stream, device))
+    with torch.cuda.device(device):
+        if out is None:
+            out = torch.empty_like(q)
+        if return_lse and lse is None:
+            lse = torch.empty((B, Hq, T), dtype=torch.float32, device=device)
+        st = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, Hq, Hkv, T, D,
+                            int(bool(causal)), float(scale), _stream_handle(stream, device))
     if st != ATTN_OK:
         raise GbAttnError("attn_fwd", st)
     return out, lse
@@ -144,40 +167,48 @@ def paged_attn_decode(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int
     ``workspace`` (uint8 CUDA tensor) is allocated here when not given.
     """
     import torch
-    device = q.device
+    device = q.device if isinstance(q, torch.Tensor) else None
     _check_bf16("q", q, 3, device)
     _check_bf16("k_pool", k_pool, 4, device)
     _check_bf16("v_pool", v_pool, 4, device)
     for name, t in (("block_table", block_table), ("seq_lens", seq_lens)):
-        if t.dtype != torch.int32 or not t.is_contiguous() or t.device != device:
-            raise ValueError(f"{name} must be a contiguous int32 tensor on {device}")
+        _check_tensor(name, t, torch.int32, None, device)
     S, Hq, D = q.shape
     NB, Hkv, bs, D2 = k_pool.shape
     if D2 != D or v_pool.shape != k_pool.shape or block_table.dim() != 2 or \
-            block_table.shape[0] != S or seq_lens.shape != (S,):
+            block_table.shape[0] != S or tuple(seq_lens.shape) != (S,):
         raise ValueError("inconsistent paged-decode shapes")
+    if out is not None:
+        _check_tensor("out", out, torch.bfloat16, (S, Hq, D), device)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, (S, Hq), device)
+    if workspace is not None:
+        _check_tensor("workspace", workspace, torch.uint8, None, device)
+    _require_cuda(device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     need = paged_attn_decode_workspace_size(S, Hq, D, max_seq_len)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
-    if out is None:
-        out = torch.empty_like(q)
-    if return_lse and lse is None:
-        lse = torch.empty((S, Hq), dtype=torch.float32, device=device)
-    st = lib().paged_attn_decode(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
-                                 block_table.data_ptr(), seq_lens.data_ptr(), bs, S, Hq, Hkv, D,
-                                 block_table.shape[1], NB, int(max_seq_len), float(scale),
-                                 out.data_ptr(), lse.data_ptr() if lse is not None else None,
-                                 workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                 _stream_handle(stream, device))
+    with torch.cuda.device(device):
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        if out is None:
+            out = torch.empty_like(q)
+        if return_lse and lse is None:
+            lse = torch.empty((S, Hq), dtype=torch.float32, device=device)
+        st = lib().paged_attn_decode(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                                     block_table.data_ptr(), seq_lens.data_ptr(), bs, S, Hq, Hkv,
+                                     D, block_table.shape[1], NB, int(max_seq_len), float(scale),
+                                     out.data_ptr(),
+                                     lse.data_ptr() if lse is not None else None,
+                                     workspace.data_ptr(), workspace.numel(),
+                                     _stream_handle(stream, device))
     if st != ATTN_OK:
         raise GbAttnError("paged_attn_decode", st)
     return out, lse
 
 
 def attn_device_status():
-    """(status, flags): synchronises the device, reads and clears the flag word."""
+    """(status, flags): synchronises the current device, reads and clears its flag word."""
     flags = ctypes.c_uint(0)
     st = lib().attn_device_status(ctypes.byref(flags))
     return st, flags.value

@@ -1,18 +1,24 @@
 """Benchmark of the fused attention hot path on GB300.
 
 One step = one pass of the whole path over one batch of synthetic input:
-  * attn_fwd on the causal prefill workload (B=4, Hq=Hkv=16, T=2048, D=128,
-    bf16 N(0,1), scale 1/sqrt(128)) -- its TFLOP/s is the headline ``value``;
+  * attn_fwd on the long causal GQA prefill workload (B=1, Hq=32, Hkv=8,
+    T=16384, D=128, bf16 N(0,1), scale 1/sqrt(128)) -- its TFLOP/s is the
+    headline ``value`` (the largest single-GPU prefill workload);
   * paged_attn_decode on the paged workload (64 requests x 1 token, Hq=12,
     Hkv=2, D=128, 16-token blocks, lengths U[512, 8192], random block tables)
     -- reported in ``paged_decode`` as KV GB/s.
+The other prefill workloads (tiny causal, causal MHA T=2048, non-causal D=64) are
+timed the same way, each on its own, and reported under ``prefill_workloads``.
 Inputs are resident in HBM before the timed region; L2 is flushed (a 512 MiB
-write) before every step, outside the kernel events.  Kernel time is taken with
-CUDA events on the launching stream.  ``e2e`` repeats the prefill metric with
-host (pinned) buffers: the H2D copy of q/k/v and the D2H copy of O and LSE sit
-inside the timed region.
+write) before every timed launch, outside the kernel events.  Kernel time is
+taken with CUDA events on the launching stream; median, p10 and p90 over the
+steps are reported.  ``e2e`` repeats the headline metric with host (pinned)
+buffers: the H2D copy of q/k/v and the D2H copy of O and LSE sit inside the
+timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       python bench.py --workload NAME --steps K --warmup W   (one workload only,
+       no CPU baseline; the form used for profiling a single kernel)
 Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
 device (independent replicas, weak scaling); the max time over ranks is used.
 """
@@ -22,7 +28,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -39,16 +44,18 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s & % bf16 tensor peak; paged-decode KV GB/s & % HBM peak"
-PREFILL = synth.CONFIGS["prefill_mha_causal"]
+HEADLINE = synth.CONFIGS["prefill_gqa_long_causal"]
 DECODE = synth.CONFIGS["paged_decode"]
+OTHER_PREFILL = [synth.CONFIGS[n] for n in ("tiny_causal", "prefill_mha_causal", "noncausal_d64")]
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
 def workload_name():
-    return (f"causal prefill MHA B={PREFILL.B} Hq=Hkv={PREFILL.Hq} T={PREFILL.T} D={PREFILL.D} "
-            f"bf16 + paged decode {DECODE.num_seqs} req x1 token Hq={DECODE.Hq} Hkv={DECODE.Hkv} "
-            f"D={DECODE.D} block_size={DECODE.block_size} L~U[{DECODE.len_lo},{DECODE.len_hi}]")
+    c, d = HEADLINE, DECODE
+    return (f"long causal GQA prefill B={c.B} Hq={c.Hq} Hkv={c.Hkv} T={c.T} D={c.D} bf16 "
+            f"+ paged decode {d.num_seqs} req x1 token Hq={d.Hq} Hkv={d.Hkv} D={d.D} "
+            f"block_size={d.block_size} L~U[{d.len_lo},{d.len_hi}]")
 
 
 def load_peaks():
@@ -70,18 +77,25 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+def load_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
             d = json.load(fh)
-        ent = d[kernel]
+        ent = d[key]
         if ent.get("source_sha") != kernel_source_sha():
             return None
         return float(ent["dram_bytes_per_launch"])
     except Exception:
         return None
+
+
+def stats(ms):
+    """median / p10 / p90 / mean of a list of per-step milliseconds."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "mean": float(a.mean())}
 
 
 # --------------------------------------------------------------------------- #
@@ -124,7 +138,7 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
@@ -133,6 +147,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 smax.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for nm, val in zip(names, parts[5:9]):
@@ -141,32 +156,43 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # --------------------------------------------------------------------------- #
 # CPU baseline: the fp64 oracle on a bounded sample
 # --------------------------------------------------------------------------- #
-def oracle_prefill_sample(q, k, v, target_s: float, seed: int):
-    """Times the oracle on random rows of the prefill workload; returns (TFLOP/s, info)."""
+def oracle_prefill_sample(cfg, q, k, v, target_s: float, seed: int):
+    """Times the oracle on random rows of a prefill workload; returns (TFLOP/s, info)."""
     import oracle
     lib = oracle.load()
-    cfg = PREFILL
-    # calibration on a small sample, then a sample sized for ~target_s
-    n = 64
+    total = cfg.B * cfg.Hq * cfg.T
+    n = 16
     while True:
-        rows = np.sort(synth.uniform_ints(seed, n, 0, cfg.B * cfg.Hq * cfg.T - 1))
+        rows = np.sort(synth.uniform_ints(seed, n, 0, total - 1))
         t0 = time.perf_counter()
         oracle.attn_rows(q, k, v, cfg.causal, cfg.softmax_scale, rows, lib=lib)
         dt = time.perf_counter() - t0
-        if dt >= target_s or n >= cfg.B * cfg.Hq * cfg.T:
+        if dt >= target_s or n >= total:
             break
-        n = int(min(cfg.B * cfg.Hq * cfg.T, max(2 * n, n * target_s / max(dt, 1e-3) * 1.05)))
+        n = int(min(total, max(2 * n, n * target_s / max(dt, 1e-3) * 1.05)))
     i = rows % cfg.T
     vis = (i + 1) if cfg.causal else np.full_like(i, cfg.T)
     flops = float(np.sum(4.0 * vis * cfg.D))  # q.k and p.v multiply-adds of each sampled row
     return flops / dt / 1e12, {"rows": int(n), "seconds": dt, "flops": flops,
                                "cores": oracle.num_threads(lib)}
+
+
+def oracle_decode_full(pg, cfg):
+    """Times the oracle's paged decode on the whole decode workload; returns (GB/s, seconds)."""
+    import oracle
+    lib = oracle.load()
+    t0 = time.perf_counter()
+    oracle.paged_decode(pg.q, pg.k_pool, pg.v_pool, pg.block_table, pg.seq_lens,
+                        cfg.softmax_scale, lib=lib)
+    dt = time.perf_counter() - t0
+    return pg.kv_bytes(cfg.Hkv, cfg.D) / dt / 1e9, dt, oracle.num_threads(lib)
 
 
 def max_over_ranks(values, device=None):
@@ -186,55 +212,105 @@ def aggregate_value(flops_per_rank: float, ms_max: float, world: int) -> float:
     return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
+def decode_bytes(pg, cfg) -> int:
+    """Algorithmic bytes of one decode launch: K/V of every cached token plus q, o, lse,
+    the block-table entries in use and seq_lens."""
+    used_blocks = int(sum(-(-int(L) // cfg.block_size) for L in pg.seq_lens))
+    return (pg.kv_bytes(cfg.Hkv, cfg.D) + pg.q.nbytes * 2 + cfg.num_seqs * cfg.Hq * 4
+            + 4 * used_blocks + pg.seq_lens.nbytes)
+
+
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
+class Runner:
+    def __init__(self, dev):
+        import torch
+        import attention_flashattention_fwd_03_gb300 as gb
+        self.gb = gb
+        self.torch = torch
+        self.dev = dev
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def to_dev(self, bits):
+        t = self.torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+        return t.view(self.torch.bfloat16).to(self.dev)
+
+    def i32(self, a):
+        return self.torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(self.dev)
+
+    def prefill_call(self, cfg, host=None):
+        torch = self.torch
+        qn, kn, vn = host if host is not None else synth.prefill_inputs(cfg)
+        q, k, v = self.to_dev(qn), self.to_dev(kn), self.to_dev(vn)
+        o = torch.empty_like(q)
+        lse = torch.empty((cfg.B, cfg.Hq, cfg.T), dtype=torch.float32, device=self.dev)
+        gb = self.gb
+
+        def call():
+            gb.attn_fwd(q, k, v, causal=cfg.causal, scale=cfg.softmax_scale, out=o, lse=lse)
+        return call, (q, k, v, o, lse)
+
+    def decode_call(self, cfg, pg):
+        torch = self.torch
+        dq, dk, dv = self.to_dev(pg.q), self.to_dev(pg.k_pool), self.to_dev(pg.v_pool)
+        dbt, dsl = self.i32(pg.block_table), self.i32(pg.seq_lens)
+        do = torch.empty_like(dq)
+        dlse = torch.empty((cfg.num_seqs, cfg.Hq), dtype=torch.float32, device=self.dev)
+        ws = torch.empty(self.gb.paged_attn_decode_workspace_size(cfg.num_seqs, cfg.Hq, cfg.D,
+                                                                  pg.max_seq_len),
+                         dtype=torch.uint8, device=self.dev)
+        gb = self.gb
+
+        def call():
+            gb.paged_attn_decode(dq, dk, dv, dbt, dsl, pg.max_seq_len, scale=cfg.softmax_scale,
+                                 out=do, lse=dlse, workspace=ws)
+        return call
+
+    def time_calls(self, calls, steps, warmup):
+        """Times each callable of ``calls`` once per step (L2 flushed before each);
+        returns one list of per-step milliseconds per callable."""
+        torch = self.torch
+        for _ in range(warmup):
+            for c in calls:
+                self.flush.zero_()
+                c()
+        torch.cuda.synchronize()
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in calls] for _ in range(steps)]
+        for i in range(steps):
+            for j, c in enumerate(calls):
+                self.flush.zero_()
+                ev[i][j][0].record(self.stream)
+                c()
+                ev[i][j][1].record(self.stream)
+        torch.cuda.synchronize()
+        return [[ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(steps)]
+                for j in range(len(calls))]
+
+    def check_status(self, when):
+        st, flags = self.gb.attn_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} flags {flags} {when}")
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import attention_flashattention_fwd_03_gb300 as gb
     gb.lib()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    R = Runner(dev)
 
-    def to_dev(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
-
-    def i32(a):
-        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
-
-    # ---- inputs (seeded, resident in HBM) ----
-    qn, kn, vn = synth.prefill_inputs(PREFILL)
-    q, k, v = to_dev(qn), to_dev(kn), to_dev(vn)
-    o = torch.empty_like(q)
-    lse = torch.empty((PREFILL.B, PREFILL.Hq, PREFILL.T), dtype=torch.float32, device=dev)
+    # ---- headline step: long causal GQA prefill + paged decode ----
+    host_pre = synth.prefill_inputs(HEADLINE)
+    pre_call, pre_bufs = R.prefill_call(HEADLINE, host_pre)
     pg = synth.paged_inputs(DECODE)
-    dq, dk, dv = to_dev(pg.q), to_dev(pg.k_pool), to_dev(pg.v_pool)
-    dbt, dsl = i32(pg.block_table), i32(pg.seq_lens)
-    do = torch.empty_like(dq)
-    dlse = torch.empty((DECODE.num_seqs, DECODE.Hq), dtype=torch.float32, device=dev)
-    ws = torch.empty(gb.paged_attn_decode_workspace_size(DECODE.num_seqs, DECODE.Hq, DECODE.D,
-                                                         pg.max_seq_len), dtype=torch.uint8,
-                     device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    dec_call = R.decode_call(DECODE, pg)
+    R.time_calls([pre_call, dec_call], 0, max(args.warmup, 3))
+    R.check_status("after warm-up")
 
-    def prefill():
-        gb.attn_fwd(q, k, v, causal=True, scale=PREFILL.softmax_scale, out=o, lse=lse)
-
-    def decode():
-        gb.paged_attn_decode(dq, dk, dv, dbt, dsl, pg.max_seq_len, scale=DECODE.softmax_scale,
-                             out=do, lse=dlse, workspace=ws)
-
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        prefill()
-        decode()
-    torch.cuda.synchronize()
-    st, flags = gb.attn_device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} flags {flags} after warm-up")
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
@@ -243,81 +319,86 @@ def run_ours(args, rank, world, local_rank):
         sampler.start()
         time.sleep(0.3)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        prefill()
-        ev[i][1].record(stream)
-        decode()
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
+    t_pre, t_dec = R.time_calls([pre_call, dec_call], args.steps, 0)
     wall = time.perf_counter() - wall0
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
-    t_pre = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    t_dec = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    launches = args.steps * 3  # 1 prefill kernel + split + merge per step
-    st, flags = gb.attn_device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} flags {flags} after timing")
+    R.check_status("after timing")
+
+    # ---- the other prefill workloads, each timed on its own ----
+    other = {}
+    for cfg in OTHER_PREFILL:
+        call, bufs = R.prefill_call(cfg)
+        (t,) = R.time_calls([call], args.steps, max(args.warmup, 3))
+        other[cfg.name] = t
+        del bufs, call
+    R.check_status("after the other workloads")
 
     # ---- e2e: host buffers, copies inside the timed region ----
-    hq = torch.from_numpy(qn.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hk = torch.from_numpy(kn.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hv = torch.from_numpy(vn.view(np.int16)).view(torch.bfloat16).pin_memory()
+    q, k, v, o, lse = pre_bufs
+    pin = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()  # noqa: E731
+    hq, hk, hv = pin(host_pre[0]), pin(host_pre[1]), pin(host_pre[2])
     ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
     hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 10))
-    e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
-    for i in range(-2, e2e_steps):
-        flush.zero_()
-        if i >= 0:
-            e_ev[i][0].record(stream)
+
+    def e2e_call():
         q.copy_(hq, non_blocking=True)
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
-        prefill()
+        pre_call()
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
-        if i >= 0:
-            e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    t_e2e = [e_ev[i][0].elapsed_time(e_ev[i][1]) for i in range(e2e_steps)]
+    e2e_steps = max(3, min(args.steps, 10))
+    (t_e2e,) = R.time_calls([e2e_call], e2e_steps, 2)
     h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
     d2h = ho.numel() * 2 + hl.numel() * 4
 
-    # ---- aggregate over ranks ----
-    ms_pre = statistics.mean(t_pre)
-    ms_dec = statistics.mean(t_dec)
-    ms_e2e = statistics.mean(t_e2e)
-    ms_pre, ms_dec, ms_e2e, wall = max_over_ranks([ms_pre, ms_dec, ms_e2e, wall], dev)
+    # ---- aggregate over ranks (max of medians) ----
+    names = ["pre", "dec", "e2e"] + list(other)
+    meds = [stats(t_pre)["median"], stats(t_dec)["median"], stats(t_e2e)["median"]] + \
+        [stats(other[n])["median"] for n in other]
+    meds_max = max_over_ranks(meds + [wall], dev)
+    med = dict(zip(names, meds_max[:-1]))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tf, info = oracle_prefill_sample(qn, kn, vn, args.cpu_seconds, PREFILL.seed + 77)
+        tf, info = oracle_prefill_sample(HEADLINE, *host_pre, args.cpu_seconds,
+                                         HEADLINE.seed + 77)
+        gbs, dsec, dcores = oracle_decode_full(pg, DECODE)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": info["cores"], "kind": "oracle",
-               "sample": (f"{info['rows']} random query rows of the prefill workload "
-                          f"({info['flops'] / 1e9:.1f} GFLOP of q.k and p.v in fp64) "
-                          f"in {info['seconds']:.1f} s")}
-    return dict(ms_pre=ms_pre, ms_dec=ms_dec, ms_e2e=ms_e2e, wall=wall, clocks=clocks,
-                launches=launches, h2d=h2d, d2h=d2h, cpu=cpu,
-                kv_bytes=pg.kv_bytes(DECODE.Hkv, DECODE.D),
-                dec_other_bytes=(pg.q.nbytes * 2 + DECODE.num_seqs * DECODE.Hq * 4
-                                 + 4 * int(sum(-(-int(L) // 16) for L in pg.seq_lens))
-                                 + pg.seq_lens.nbytes),
-                t_pre=t_pre, t_dec=t_dec)
+               "sample": (f"{info['rows']} random query rows of the long causal GQA prefill "
+                          f"workload ({info['flops'] / 1e9:.1f} GFLOP of q.k and p.v in fp64) "
+                          f"in {info['seconds']:.1f} s"),
+               "paged_decode": {"value": gbs, "unit": "GB/s", "cores": dcores, "kind": "oracle",
+                                "sample": f"the whole paged decode workload in {dsec:.2f} s"}}
+    return dict(med=med, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e, other=other,
+                wall=meds_max[-1], clocks=clocks, launches=args.steps * 3,
+                h2d=h2d, d2h=d2h, cpu=cpu, dec_bytes=decode_bytes(pg, DECODE),
+                kv_bytes=pg.kv_bytes(DECODE.Hkv, DECODE.D))
+
+
+def prefill_entry(cfg, ms_list, ms_med, peaks, src):
+    tf = cfg.flops() / (ms_med * 1e-3) / 1e12
+    s = stats(ms_list)
+    return {"B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "T": cfg.T, "D": cfg.D,
+            "causal": cfg.causal, "flops": cfg.flops(), "flops_exact": cfg.flops_exact(),
+            "tflops": round(tf, 2),
+            "frac": round(tf / peaks["bf16_tflops"], 4),
+            "frac_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+            "peak_source": f"{src} dense bf16",
+            "ms": {k: round(v, 5) for k, v in s.items()}}
 
 
 def report_ours(args, res, world):
     peaks, src = load_peaks()
-    flops = PREFILL.flops()
-    tf_rank = flops / (res["ms_pre"] * 1e-3) / 1e12
-    value = aggregate_value(flops, res["ms_pre"], world)
-    frac = tf_rank / peaks["bf16_tflops"]
-    dec_bytes = res["kv_bytes"] + res["dec_other_bytes"]
-    gbs = dec_bytes / (res["ms_dec"] * 1e-3) / 1e9
-    e2e_tf = world * flops / (res["ms_e2e"] * 1e-3) / 1e12
+    med = res["med"]
+    flops = HEADLINE.flops()
+    tf_rank = flops / (med["pre"] * 1e-3) / 1e12
+    value = aggregate_value(flops, med["pre"], world)
+    gbs = res["dec_bytes"] / (med["dec"] * 1e-3) / 1e9
+    e2e_tf = world * flops / (med["e2e"] * 1e-3) / 1e12
+    kname = f"attn_fwd_kernel<{HEADLINE.D}>"
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -325,7 +406,7 @@ def report_ours(args, res, world):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(res["ms_pre"] + res["ms_dec"], 5),
+        "ms_per_step": round(med["pre"] + med["dec"], 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -333,43 +414,50 @@ def report_ours(args, res, world):
         "data": "synthetic (seeded N(0,1) bf16; paged pool with random block tables)",
         "config": {
             "workload": workload_name(),
-            "prefill": {"B": PREFILL.B, "Hq": PREFILL.Hq, "Hkv": PREFILL.Hkv, "T": PREFILL.T,
-                        "D": PREFILL.D, "causal": True, "flops_per_step": flops,
+            "prefill": {"B": HEADLINE.B, "Hq": HEADLINE.Hq, "Hkv": HEADLINE.Hkv,
+                        "T": HEADLINE.T, "D": HEADLINE.D, "causal": True,
+                        "flops_per_step": flops,
                         "flop_convention": "4*B*Hq*T^2*D/2 (causal half)",
-                        "flops_exact_causal": PREFILL.flops_exact()},
+                        "flops_exact_causal": HEADLINE.flops_exact()},
             "decode": {"num_seqs": DECODE.num_seqs, "Hq": DECODE.Hq, "Hkv": DECODE.Hkv,
                        "D": DECODE.D, "block_size": DECODE.block_size,
                        "seq_len_range": [DECODE.len_lo, DECODE.len_hi]},
-            "l2": "flushed before every step (512 MiB write, outside the kernel events)",
+            "l2": "flushed before every timed launch (512 MiB write, outside the kernel events)",
+            "timing": "CUDA events on the launching stream; value from the median step",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
-        "prefill_ms": round(res["ms_pre"], 5),
+        "prefill_ms": {k: round(v, 5) for k, v in stats(res["t_pre"]).items()},
         "roofline": {
-            "kernel": "attn_fwd_kernel<128>",
+            "kernel": kname,
             "bound": "tensor",
             "achieved": round(tf_rank, 2),
             "peak": peaks["bf16_tflops"],
-            "peak_source": f"{src} dense bf16 (burst)",
+            "peak_source": f"{src} dense bf16 (burst; the kernel is timed alone)",
             "unit": "TFLOP/s",
-            "frac": round(frac, 4),
-            "traffic": load_traffic("attn_fwd_kernel<128>"),
-            "algorithmic_bytes": PREFILL.io_bytes(),
+            "frac": round(tf_rank / peaks["bf16_tflops"], 4),
+            "frac_of_sustained": round(tf_rank / peaks["bf16_tflops_sustained"], 4),
+            "traffic": load_traffic(f"{kname} {HEADLINE.name}"),
+            "algorithmic_bytes": HEADLINE.io_bytes(),
         },
+        "prefill_workloads": {
+            cfg.name: prefill_entry(cfg, res["other"][cfg.name], med[cfg.name], peaks, src)
+            for cfg in OTHER_PREFILL},
         "paged_decode": {
             "value": round(gbs, 1),
             "unit": "GB/s",
-            "ms": round(res["ms_dec"], 5),
+            "ms": {k: round(v, 5) for k, v in stats(res["t_dec"]).items()},
             "kv_bytes": res["kv_bytes"],
-            "bytes_per_step": dec_bytes,
-            "roofline": {"kernel": "paged_decode_split_kernel<128> + merge", "bound": "hbm",
-                         "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+            "bytes_per_step": res["dec_bytes"],
+            "roofline": {"kernel": f"paged_decode_split_kernel<{DECODE.D}> + merge",
+                         "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "peak_source": f"{src} copy bandwidth", "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4),
-                         "traffic": load_traffic("paged_decode_split_kernel<128>")},
+                         "traffic": load_traffic(f"paged_decode {DECODE.name}")},
         },
         "e2e": {"value": round(e2e_tf, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
-                "ms_per_step": round(res["ms_e2e"], 4)},
+                "ms_per_step": round(med["e2e"], 4),
+                "what": "attn_fwd on the headline workload from pinned host buffers"},
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "wall_s_timed": round(res["wall"], 4),
@@ -379,20 +467,43 @@ def report_ours(args, res, world):
     return line
 
 
+def run_single(args, local_rank):
+    """One workload only (for profiling): W warm-up launches, then K timed ones."""
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    R = Runner(dev)
+    name = args.workload
+    if name == DECODE.name:
+        pg = synth.paged_inputs(DECODE)
+        call = R.decode_call(DECODE, pg)
+        work, unit = decode_bytes(pg, DECODE) / 1e9, "GB/s"
+    else:
+        cfg = synth.CONFIGS[name]
+        call, _bufs = R.prefill_call(cfg)
+        work, unit = cfg.flops() / 1e12, "TFLOP/s"
+    (t,) = R.time_calls([call], args.steps, args.warmup)
+    R.check_status("after the single workload")
+    s = stats(t)
+    print(json.dumps({"workload": name, "value": round(work / (s["median"] * 1e-3), 2),
+                      "unit": unit, "ms": s, "steps": args.steps, "warmup": args.warmup}),
+          flush=True)
+
+
 # --------------------------------------------------------------------------- #
 # reference arm: the fp64 oracle on the host cores
 # --------------------------------------------------------------------------- #
 def run_reference(args):
-    qn, kn, vn = synth.prefill_inputs(PREFILL)
+    qn, kn, vn = synth.prefill_inputs(HEADLINE)
     per_step = max(0.5, min(10.0, args.ref_budget_s / max(1, args.steps + args.warmup)))
     tfs = []
     info = None
     for i in range(args.warmup + args.steps):
-        tf, info = oracle_prefill_sample(qn, kn, vn, per_step, PREFILL.seed + 1000 + i)
+        tf, info = oracle_prefill_sample(HEADLINE, qn, kn, vn, per_step, HEADLINE.seed + 1000 + i)
         if i >= args.warmup:
             tfs.append(tf)
-    value = statistics.mean(tfs)
-    flops = PREFILL.flops()
+    value = statistics.median(tfs)
+    flops = HEADLINE.flops()
     return {
         "metric": METRIC,
         "impl": "reference",
@@ -408,8 +519,8 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 inputs widened to fp64)",
         "config": {"workload": workload_name(), "note": "each step times the fp64 CPU oracle on "
-                   "a bounded random sample of query rows of the prefill workload; ms_per_step "
-                   "is the extrapolated time of a full step"},
+                   "a bounded random sample of query rows of the long causal GQA prefill "
+                   "workload; ms_per_step is the extrapolated time of a full prefill"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": info["cores"],
                          "kind": "oracle",
                          "sample": f"{info['rows']} random query rows per step"},
@@ -424,11 +535,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(synth.CONFIGS), default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -438,6 +549,10 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
+    if args.workload is not None:
+        run_single(args, local_rank)
+        return
+    args.warmup = max(args.warmup, 3)
 
     if world > 1:
         import torch

@@ -47,17 +47,3 @@ def check_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
         assert np.all(np.isfinite(lse_gpu)), f"{what}: non-finite LSE"
         assert lerr.max() <= LSE_MAX_ABS, f"{what}: LSE max-abs {lerr.max():.3e}"
     return float(err.max()), float(err.mean())
-
-
-def sample_rows(B, Hq, T, n, seed):
-    """Flat row indices ((b*Hq)+h)*T+i: tile edges of every head plus random rows."""
-    rows = set()
-    edges = [0, 1, 126, 127, 128, 129, T - 129, T - 128, T - 2, T - 1]
-    heads = [(0, 0), (B - 1, Hq - 1), (B // 2, Hq // 2)]
-    for b, h in heads:
-        for i in edges:
-            if 0 <= i < T:
-                rows.add((b * Hq + h) * T + i)
-    rnd = synth.uniform_ints(seed, n, 0, B * Hq * T - 1)
-    rows.update(int(x) for x in rnd)
-    return np.array(sorted(rows), dtype=np.int64)

@@ -127,3 +127,61 @@ def test_valid_call_without_a_device_is_an_error_not_a_fallback(lib):
         pytest.skip("a device is present; this checks the no-device path")
     assert fwd(lib) == gb.ATTN_ERR_CUDA
     assert dec(lib) == gb.ATTN_ERR_CUDA
+
+
+# --------------------------------------------------------------------------- #
+# the Python binding's checks (metadata only: they run before any device work)
+# --------------------------------------------------------------------------- #
+def _bf16(*shape):
+    torch = pytest.importorskip("torch")
+    return torch.zeros(shape, dtype=torch.bfloat16)
+
+
+def _f32(*shape):
+    torch = pytest.importorskip("torch")
+    return torch.zeros(shape, dtype=torch.float32)
+
+
+@pytest.mark.parametrize("bad", ["out_shape", "out_dtype", "lse_shape", "lse_dtype",
+                                 "lse_strided", "cpu_tensors", "k_mismatch"])
+def test_binding_rejects_bad_attn_fwd_tensors(bad):
+    q, k, v = _bf16(1, 2, 8, 64), _bf16(1, 1, 8, 64), _bf16(1, 1, 8, 64)
+    kw = {}
+    if bad == "out_shape":
+        kw["out"] = _bf16(1, 2, 8, 32)
+    elif bad == "out_dtype":
+        kw["out"] = _f32(1, 2, 8, 64)
+    elif bad == "lse_shape":
+        kw["lse"] = _f32(1, 2, 9)
+    elif bad == "lse_dtype":
+        kw["lse"] = _bf16(1, 2, 8)
+    elif bad == "lse_strided":
+        kw["lse"] = _f32(1, 2, 16)[:, :, ::2]
+    elif bad == "k_mismatch":
+        k = _bf16(1, 1, 7, 64)
+    with pytest.raises(ValueError):
+        gb.attn_fwd(q, k, v, **kw)
+
+
+@pytest.mark.parametrize("bad", ["out_shape", "out_dtype", "lse_shape", "lse_dtype",
+                                 "table_dtype", "ws_dtype", "cpu_tensors"])
+def test_binding_rejects_bad_decode_tensors(bad):
+    torch = pytest.importorskip("torch")
+    q, kp, vp = _bf16(2, 4, 64), _bf16(10, 2, 16, 64), _bf16(10, 2, 16, 64)
+    bt = torch.zeros((2, 4), dtype=torch.int32)
+    sl = torch.ones(2, dtype=torch.int32)
+    kw = {}
+    if bad == "out_shape":
+        kw["out"] = _bf16(2, 4, 32)
+    elif bad == "out_dtype":
+        kw["out"] = _f32(2, 4, 64)
+    elif bad == "lse_shape":
+        kw["lse"] = _f32(2, 5)
+    elif bad == "lse_dtype":
+        kw["lse"] = _bf16(2, 4)
+    elif bad == "table_dtype":
+        bt = bt.to(torch.int64)
+    elif bad == "ws_dtype":
+        kw["workspace"] = _f32(64)
+    with pytest.raises(ValueError):
+        gb.paged_attn_decode(q, kp, vp, bt, sl, 64, **kw)

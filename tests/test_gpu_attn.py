@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import check_close, from_dev, bits_of, sample_rows, to_dev
+from gpu_util import check_close, from_dev, bits_of, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -60,20 +60,22 @@ def test_attn_fwd_matches_oracle_small(gb, B, Hq, Hkv, T, D, causal):
 
 
 @pytest.mark.parametrize("name", ["prefill_mha_causal", "prefill_gqa_long_causal", "noncausal_d64"])
-def test_attn_fwd_full_size_sampled_rows(gb, name):
+def test_attn_fwd_full_size_every_row(gb, name):
+    """The full-size workloads against the oracle on every output element.
+
+    The error bounds hold over the whole of O and LSE (max and mean over all
+    rows of all heads), not over a sample.
+    """
     cfg = synth.CONFIGS[name]
     q, k, v = synth.prefill_inputs(cfg)
     o, lse = run(gb, q, k, v, cfg.causal, cfg.softmax_scale)
-    rows = sample_rows(cfg.B, cfg.Hq, cfg.T, 384, cfg.seed + 9)
-    o_ref, lse_ref = oracle.attn_rows(q, k, v, cfg.causal, cfg.softmax_scale, rows)
-    og = from_dev(o).reshape(-1, cfg.D)[rows]
-    lg = from_dev(lse).reshape(-1)[rows]
-    check_close(og, lg, o_ref, lse_ref, name)
-    # properties over every row: finite, and |O| bounded by max |V| of its KV head
-    of = from_dev(o)
-    assert np.all(np.isfinite(of)) and np.all(np.isfinite(from_dev(lse)))
-    vmax = np.abs(synth.bf16_bits_to_float(v)).max()
-    assert np.abs(of).max() <= vmax * (1 + 1e-2)
+    og, lg = from_dev(o), from_dev(lse)
+    del o, lse
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, cfg.causal, cfg.softmax_scale)
+    mx, mean = check_close(og, lg, o_ref, lse_ref, name)
+    lmx = float(np.abs(lg - lse_ref).max())
+    print(f"PARITY {name} rows={og.size // cfg.D} o_max_abs={mx:.3e} o_mean_abs={mean:.3e} "
+          f"lse_max_abs={lmx:.3e}")
 
 
 def test_first_causal_row_is_v0_bit_exact(gb):

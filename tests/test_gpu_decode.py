@@ -43,7 +43,10 @@ def test_decode_full_size_matches_oracle(gb, cfg5):
     o, lse = run(gb, p, cfg.softmax_scale)
     o_ref, lse_ref = oracle.paged_decode(p.q, p.k_pool, p.v_pool, p.block_table, p.seq_lens,
                                          cfg.softmax_scale)
-    check_close(from_dev(o), from_dev(lse), o_ref, lse_ref, "paged_decode")
+    of, lf = from_dev(o), from_dev(lse)
+    mx, mean = check_close(of, lf, o_ref, lse_ref, "paged_decode")
+    print(f"PARITY paged_decode rows={of.size // cfg.D} o_max_abs={mx:.3e} o_mean_abs={mean:.3e} "
+          f"lse_max_abs={float(np.abs(lf - lse_ref).max()):.3e}")
 
 
 def test_decode_placement_invariance_bit_exact(gb, cfg5):
