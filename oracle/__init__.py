@@ -155,6 +155,27 @@ def paged_decode(q, k_pool, v_pool, block_table, seq_lens, scale: float, lib=Non
     return o, lse
 
 
+def paged_prefill(q, k_pool, v_pool, block_table, kv_lens, causal: bool, scale: float, lib=None):
+    """O [B,Hq,Tq,D] float64 and LSE [B,Hq,Tq] of a chunk of Tq queries per batch item
+    against that item's paged cache of kv_lens[b] tokens (the chunk being its newest
+    tokens).  Composes the oracle's block-table gather with its attention: each
+    item's K/V history is gathered through the table, then attended to with
+    Tq != Tk (bottom-right causal alignment)."""
+    lib = lib or load()
+    q = _u16(q)
+    B, Hq, Tq, D = q.shape
+    NB, Hkv, bs, D2 = k_pool.shape
+    kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
+    o = np.zeros((B, Hq, Tq, D), dtype=np.float64)
+    lse = np.zeros((B, Hq, Tq), dtype=np.float64)
+    for b in range(B):
+        kc = np.stack([paged_gather(k_pool, block_table, kl, b, h, lib=lib) for h in range(Hkv)])
+        vc = np.stack([paged_gather(v_pool, block_table, kl, b, h, lib=lib) for h in range(Hkv)])
+        ob, lb = attn_fwd(q[b:b + 1], kc[None], vc[None], causal, scale, lib=lib)
+        o[b], lse[b] = ob[0], lb[0]
+    return o, lse
+
+
 def num_threads(lib=None) -> int:
     lib = lib or load()
     return int(lib.oracle_num_threads())

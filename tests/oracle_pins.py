@@ -85,6 +85,69 @@ def pin_bruteforce_highprecision(lib):
             assert np.abs(lse - el).max() <= 1e-13, ("LSE", B, Hq, Hkv, T, D, causal)
 
 
+def _mp_rect(qf, kf, vf, causal, scale, group):
+    """40-digit brute force for Tq query rows against Tk keys.  The Tq queries are
+    the newest tokens of a Tk-token sequence, so query i sits at position
+    Tk - Tq + i and, when causal, sees keys 0 .. Tk - Tq + i; a query that sees
+    no key gives O = 0 and LSE = -inf."""
+    import mpmath as mp
+    mp.mp.dps = 40
+    B, Hq, Tq, D = qf.shape
+    Tk = kf.shape[2]
+    o = np.zeros(qf.shape)
+    lse = np.zeros((B, Hq, Tq))
+    sc = mp.mpf(scale)
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // group
+            for i in range(Tq):
+                pos = Tk - Tq + i
+                keys = [j for j in range(Tk) if (not causal or j <= pos)]
+                if not keys:
+                    lse[b, h, i] = -np.inf
+                    continue
+                e = [mp.exp(sc * mp.fsum(mp.mpf(float(qf[b, h, i, d])) * mp.mpf(float(kf[b, kv, j, d]))
+                                         for d in range(D))) for j in keys]
+                tot = mp.fsum(e)
+                for d in range(D):
+                    o[b, h, i, d] = float(mp.fsum(e[n] * mp.mpf(float(vf[b, kv, j, d]))
+                                                  for n, j in enumerate(keys)) / tot)
+                lse[b, h, i] = float(mp.log(tot))
+    return o, lse
+
+
+def pin_bottom_right_bruteforce(lib):
+    """Tq != Tk: the queries are the last Tq tokens (chunked prefill / decode)."""
+    cases = [(1, 2, 1, 2, 5, 3), (1, 2, 2, 1, 4, 2), (2, 4, 2, 3, 7, 2), (1, 2, 1, 5, 3, 2),
+             (1, 1, 1, 4, 4, 3)]
+    for n, (B, Hq, Hkv, Tq, Tk, D) in enumerate(cases):
+        for causal in (True, False):
+            seed = 7600 + 10 * n + causal
+            q = synth.normal_bf16(seed, (B, Hq, Tq, D))
+            k = synth.normal_bf16(seed + 1, (B, Hkv, Tk, D), 2.0)
+            v = synth.normal_bf16(seed + 2, (B, Hkv, Tk, D))
+            o, lse = oracle.attn_fwd(q, k, v, causal, 0.6, lib=lib)
+            eo, el = _mp_rect(f32(q), f32(k), f32(v), causal, 0.6, Hq // Hkv)
+            assert np.abs(o - eo).max() <= 1e-13, ("O", Tq, Tk, causal)
+            fin = np.isfinite(el)
+            assert np.array_equal(np.isneginf(lse), ~fin), ("empty rows", Tq, Tk, causal)
+            assert np.abs(lse[fin] - el[fin]).max() <= 1e-13, ("LSE", Tq, Tk, causal)
+
+
+def pin_chunk_is_tail_of_full(lib):
+    """Causal attention of the last Tq queries against all Tk keys equals the last Tq
+    rows of causal attention of the whole Tk-token sequence, bit for bit."""
+    B, Hq, Hkv, Tk, D = 1, 4, 2, 70, 16
+    qfull = synth.normal_bf16(7700, (B, Hq, Tk, D))
+    k = synth.normal_bf16(7701, (B, Hkv, Tk, D))
+    v = synth.normal_bf16(7702, (B, Hkv, Tk, D))
+    of, lf = oracle.attn_fwd(qfull, k, v, True, 0.3, lib=lib)
+    for Tq in (1, 2, 17, 69, 70):
+        o, lse = oracle.attn_fwd(np.ascontiguousarray(qfull[:, :, Tk - Tq:]), k, v, True, 0.3,
+                                 lib=lib)
+        assert np.array_equal(o, of[:, :, Tk - Tq:]) and np.array_equal(lse, lf[:, :, Tk - Tq:]), Tq
+
+
 # --------------------------------------------------------------------------- #
 # 2. library special case: torch SDPA (fp64, CPU) and scipy logsumexp
 # --------------------------------------------------------------------------- #
@@ -329,6 +392,34 @@ def pin_paged_empty_request(lib):
     assert np.all(np.isfinite(o[1])) and np.all(np.isfinite(lse[1]))
 
 
+def pin_paged_prefill_is_gather_then_attention(lib):
+    """Chunked prefill through the table equals attention over the gathered K/V with
+    the chunk as the newest tokens; with one query it is paged decode, bit for bit."""
+    cfg, p = _small_paged(8650, lens=(1, 15, 16, 17, 70))
+    B, Tq = len(p.seq_lens), 1
+    q1 = p.q[:, :, None, :].copy()
+    o, lse = oracle.paged_prefill(q1, p.k_pool, p.v_pool, p.block_table, p.seq_lens, True,
+                                  cfg.softmax_scale, lib=lib)
+    od, ld = oracle.paged_decode(p.q, p.k_pool, p.v_pool, p.block_table, p.seq_lens,
+                                 cfg.softmax_scale, lib=lib)
+    assert np.array_equal(o[:, :, 0], od) and np.array_equal(lse[:, :, 0], ld)
+    Tq = 5
+    q = synth.normal_bf16(8651, (B, cfg.Hq, Tq, cfg.D))
+    for causal in (True, False):
+        o, lse = oracle.paged_prefill(q, p.k_pool, p.v_pool, p.block_table, p.seq_lens, causal,
+                                      cfg.softmax_scale, lib=lib)
+        for b in range(B):
+            L = int(p.seq_lens[b])
+            t = np.arange(L)
+            phys = p.block_table[b, t // p.block_size]
+            kc = np.stack([p.k_pool[phys, h, t % p.block_size] for h in range(cfg.Hkv)])[None]
+            vc = np.stack([p.v_pool[phys, h, t % p.block_size] for h in range(cfg.Hkv)])[None]
+            oc, lc = oracle.attn_fwd(q[b:b + 1], kc, vc, causal, cfg.softmax_scale, lib=lib)
+            assert np.array_equal(oc[0], o[b]) and np.array_equal(lc[0], lse[b]), (b, causal)
+        if causal:  # request 0 has one key: only its last query sees it
+            assert np.all(o[0, :, :Tq - 1] == 0) and np.all(np.isneginf(lse[0, :, :Tq - 1]))
+
+
 def pin_split_merge(lib):
     """Merging per-chunk (O_s, LSE_s) with weights e^{LSE_s - LSE} gives the unsplit result."""
     B, Hq, Hkv, T, D = 1, 2, 1, 1300, 16
@@ -387,6 +478,9 @@ def pin_golden_paged(lib):
 
 PINS = [
     pin_bruteforce_highprecision,
+    pin_bottom_right_bruteforce,
+    pin_chunk_is_tail_of_full,
+    pin_paged_prefill_is_gather_then_attention,
     pin_library_sdpa,
     pin_rows_sum_to_one,
     pin_constant_v,

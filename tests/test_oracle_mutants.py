@@ -16,6 +16,8 @@ from oracle_pins import PINS
 MUTANTS = {
     "causal_off_by_one": ("long long n = (long long)i + (Tk - Tq) + 1;",
                           "long long n = (long long)i + (Tk - Tq);"),
+    "causal_top_left_when_rectangular": ("long long n = (long long)i + (Tk - Tq) + 1;",
+                                         "long long n = (long long)i + 1;"),
     "gqa_head_modulo": ("const int kvh = h / group;\n                const uint16_t *qrow",
                         "const int kvh = h % Hkv;\n                const uint16_t *qrow"),
     "scale_dropped": ("p[j] = scale * acc;", "p[j] = acc;"),
