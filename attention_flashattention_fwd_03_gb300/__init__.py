@@ -30,6 +30,7 @@ EXPORTS = (
     "attn_fwd",
     "paged_attn_decode_workspace_size",
     "paged_attn_decode",
+    "paged_attn_decode_noalloc",
     "attn_device_status",
     "attn_version",
 )
@@ -71,6 +72,8 @@ def _bind(h):
     h.paged_attn_decode_workspace_size.restype = Z
     h.paged_attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, P, P, Z, P]
     h.paged_attn_decode.restype = I
+    h.paged_attn_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, P, P]
+    h.paged_attn_decode_noalloc.restype = I
     h.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     h.attn_device_status.restype = I
     h.attn_version.argtypes = []

@@ -106,6 +106,44 @@ int paged_attn_decode(const void *q, const void *k_pool, const void *v_pool,
                       int num_pool_blocks, int max_seq_len, float scale, void *o, float *lse,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/* Bytes of device scratch paged_attn_decode_noalloc reserves on each device. */
+#define GBATTN_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * paged_attn_decode_noalloc -- paged_attn_decode without a caller workspace.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers that
+ * cannot allocate device memory at the point where they decode: code running
+ * inside an allocator's own hooks, a host application that owns every device
+ * allocation and hands out none, or a latency-critical loop that must never
+ * enter the allocator.  Such a caller still owns and passes every input and
+ * output (same arguments, layouts and checks as paged_attn_decode); only the
+ * split-KV scratch comes from the library, from one fixed array of
+ * GBATTN_DECODE_NOALLOC_SCRATCH_BYTES (16 MiB) in the library's device image.
+ * Every GPU on which the library's kernels are loaded holds that array until
+ * the process exits.  The call itself allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ *   - Sizes whose scratch, paged_attn_decode_workspace_size(num_seqs, Hq, D,
+ *     max_seq_len), exceeds the array return ATTN_ERR_UNSUPPORTED before any
+ *     work is enqueued (at D = 128 that is about 32,000 (request, query head,
+ *     512-token chunk) partial results; 64 requests x 12 heads x 8192 tokens
+ *     need 6.3 MB).
+ *   - The first call on a device looks up the array's device address (once,
+ *     with that device current); make that first call before any stream
+ *     capture begins.
+ *   - All calls on a device share the one array and it keeps whatever the last
+ *     call wrote.  Nothing in it needs to start at zero: each call writes every
+ *     scratch element it later reads.  Calls whose executions overlap on the GPU
+ *     (different streams with no ordering between them) race on the array and
+ *     give wrong results: order them on one stream or with events.
+ */
+int paged_attn_decode_noalloc(const void *q, const void *k_pool, const void *v_pool,
+                              const int32_t *block_table, const int32_t *seq_lens, int block_size,
+                              int num_seqs, int Hq, int Hkv, int D, int max_blocks_per_seq,
+                              int num_pool_blocks, int max_seq_len, float scale, void *o,
+                              float *lse, void *stream);
+
 /*
  * Synchronises the current device, then reads and clears the library's device
  * flag word.  *flags (if not NULL) receives the raw bits: 1 = a bounded wait in
