@@ -31,6 +31,10 @@ EXPORTS = (
     "paged_attn_decode_workspace_size",
     "paged_attn_decode",
     "paged_attn_decode_noalloc",
+    "paged_attn_prefill",
+    "paged_kv_append",
+    "paged_kv_gather",
+    "attn_test_set_failure",
     "attn_device_status",
     "attn_version",
 )
@@ -74,6 +78,14 @@ def _bind(h):
     h.paged_attn_decode.restype = I
     h.paged_attn_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, P, P]
     h.paged_attn_decode_noalloc.restype = I
+    h.paged_attn_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, P, P, P]
+    h.paged_attn_prefill.restype = I
+    h.paged_kv_append.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P]
+    h.paged_kv_append.restype = I
+    h.paged_kv_gather.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P]
+    h.paged_kv_gather.restype = I
+    h.attn_test_set_failure.argtypes = [ctypes.c_ulonglong, I]
+    h.attn_test_set_failure.restype = I
     h.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     h.attn_device_status.restype = I
     h.attn_version.argtypes = []
@@ -208,6 +220,120 @@ def paged_attn_decode(q, k_pool, v_pool, block_table, seq_lens, max_seq_len: int
     if st != ATTN_OK:
         raise GbAttnError("paged_attn_decode", st)
     return out, lse
+
+
+def paged_attn_prefill(q, k_pool, v_pool, block_table, kv_lens, max_kv_len: int,
+                       causal: bool = True, scale: float | None = None, out=None, lse=None,
+                       return_lse: bool = True, stream=None):
+    """Chunked prefill against a paged KV cache through the C ABI.
+
+    q [B,Hq,Tq,D] bf16 (the Tq newest tokens of each item), k_pool/v_pool
+    [NB,Hkv,16,D] bf16, block_table [B,max_blocks] int32, kv_lens [B] int32 (all
+    CUDA) -> (o [B,Hq,Tq,D] bf16, lse [B,Hq,Tq] fp32).  Query i of item b sits at
+    logical position kv_lens[b] - Tq + i.
+    """
+    import torch
+    device = q.device if isinstance(q, torch.Tensor) else None
+    _check_bf16("q", q, 4, device)
+    _check_bf16("k_pool", k_pool, 4, device)
+    _check_bf16("v_pool", v_pool, 4, device)
+    for name, t in (("block_table", block_table), ("kv_lens", kv_lens)):
+        _check_tensor(name, t, torch.int32, None, device)
+    B, Hq, Tq, D = q.shape
+    NB, Hkv, bs, D2 = k_pool.shape
+    if D2 != D or v_pool.shape != k_pool.shape or block_table.dim() != 2 or \
+            block_table.shape[0] != B or tuple(kv_lens.shape) != (B,):
+        raise ValueError("inconsistent paged-prefill shapes")
+    if out is not None:
+        _check_tensor("out", out, torch.bfloat16, (B, Hq, Tq, D), device)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, (B, Hq, Tq), device)
+    _require_cuda(device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(device):
+        if out is None:
+            out = torch.empty_like(q)
+        if return_lse and lse is None:
+            lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=device)
+        st = lib().paged_attn_prefill(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                                      block_table.data_ptr(), kv_lens.data_ptr(), bs, B, Hq, Hkv,
+                                      Tq, D, block_table.shape[1], NB, int(max_kv_len),
+                                      int(bool(causal)), float(scale), out.data_ptr(),
+                                      lse.data_ptr() if lse is not None else None,
+                                      _stream_handle(stream, device))
+    if st != ATTN_OK:
+        raise GbAttnError("paged_attn_prefill", st)
+    return out, lse
+
+
+def paged_kv_append(k_new, v_new, k_pool, v_pool, block_table, seq_lens, new_seq_lens=None,
+                    stream=None):
+    """Writes the Tn new tokens of each request into the paged pools (in place).
+
+    k_new/v_new [S,Hkv,Tn,D] bf16, k_pool/v_pool [NB,Hkv,16,D] bf16, block_table
+    [S,max_blocks] int32, seq_lens [S] int32 (lengths before the append);
+    new_seq_lens [S] int32, if given, receives seq_lens + Tn.
+    """
+    import torch
+    device = k_new.device if isinstance(k_new, torch.Tensor) else None
+    _check_bf16("k_new", k_new, 4, device)
+    _check_bf16("v_new", v_new, 4, device)
+    _check_bf16("k_pool", k_pool, 4, device)
+    _check_bf16("v_pool", v_pool, 4, device)
+    for name, t in (("block_table", block_table), ("seq_lens", seq_lens)):
+        _check_tensor(name, t, torch.int32, None, device)
+    S, Hkv, Tn, D = k_new.shape
+    NB, Hkv2, bs, D2 = k_pool.shape
+    if v_new.shape != k_new.shape or v_pool.shape != k_pool.shape or Hkv2 != Hkv or D2 != D or \
+            block_table.dim() != 2 or block_table.shape[0] != S or tuple(seq_lens.shape) != (S,):
+        raise ValueError("inconsistent append shapes")
+    if new_seq_lens is not None:
+        _check_tensor("new_seq_lens", new_seq_lens, torch.int32, (S,), device)
+    _require_cuda(device)
+    with torch.cuda.device(device):
+        st = lib().paged_kv_append(k_new.data_ptr(), v_new.data_ptr(), k_pool.data_ptr(),
+                                   v_pool.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+                                   new_seq_lens.data_ptr() if new_seq_lens is not None else None,
+                                   bs, S, Hkv, Tn, D, block_table.shape[1], NB,
+                                   _stream_handle(stream, device))
+    if st != ATTN_OK:
+        raise GbAttnError("paged_kv_append", st)
+    return new_seq_lens
+
+
+def paged_kv_gather(pool, block_table, seq_lens, max_seq_len: int, out=None, stream=None):
+    """Each request's cached rows in logical order: out [S,Hkv,max_seq_len,D] bf16
+    (rows past a request's length are left as they were)."""
+    import torch
+    device = pool.device if isinstance(pool, torch.Tensor) else None
+    _check_bf16("pool", pool, 4, device)
+    for name, t in (("block_table", block_table), ("seq_lens", seq_lens)):
+        _check_tensor(name, t, torch.int32, None, device)
+    NB, Hkv, bs, D = pool.shape
+    S = seq_lens.shape[0]
+    if block_table.dim() != 2 or block_table.shape[0] != S:
+        raise ValueError("inconsistent gather shapes")
+    if out is not None:
+        _check_tensor("out", out, torch.bfloat16, (S, Hkv, max_seq_len, D), device)
+    _require_cuda(device)
+    with torch.cuda.device(device):
+        if out is None:
+            out = torch.zeros((S, Hkv, max_seq_len, D), dtype=torch.bfloat16, device=device)
+        st = lib().paged_kv_gather(pool.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+                                   bs, S, Hkv, D, block_table.shape[1], NB, int(max_seq_len),
+                                   out.data_ptr(), _stream_handle(stream, device))
+    if st != ATTN_OK:
+        raise GbAttnError("paged_kv_gather", st)
+    return out
+
+
+def test_set_failure(wait_limit_ns: int = 0, withhold_copy: bool = False) -> None:
+    """Test hook: in-kernel wait limit (0 = default 2 s) and whether the next kernels'
+    copy warps withhold their first copy so that a wait runs out."""
+    st = lib().attn_test_set_failure(int(wait_limit_ns), int(bool(withhold_copy)))
+    if st != ATTN_OK:
+        raise GbAttnError("attn_test_set_failure", st)
 
 
 def attn_device_status():

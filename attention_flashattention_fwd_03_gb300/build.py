@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgbattn.so")
-SOURCES = ["attn_fwd.cu", "paged_decode.cu", "api.cu", "decode_noalloc.cu"]
+SOURCES = ["attn_fwd.cu", "paged_decode.cu", "kv_cache.cu", "api.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -144,9 +144,15 @@ __global__ void __launch_bounds__(kThreads)
       int issued = 0;
       for (int i = 0; i < nblk; ++i) {
         const int s = i % kStages;
-        if (!mbar_wait(bar_empty + 8 * s, ((i / kStages) & 1) ^ 1, abort, p.flags)) break;
+        if (!mbar_wait(bar_empty + 8 * s, ((i / kStages) & 1) ^ 1, abort, p.flags,
+                       p.wait_limit_ns))
+          break;
         const uint32_t dst = sbase + s * C::STAGE_BYTES;
         const int row = (table[i] * p.Hkv + kvh) * kBS;
+        if (p.withhold_copy && i == 0) {  // test hook: the first block never arrives
+          ++issued;
+          continue;
+        }
         mbar_arrive_expect_tx(bar_full + 8 * s, C::STAGE_BYTES);
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb) {
@@ -157,7 +163,8 @@ __global__ void __launch_bounds__(kThreads)
       }
       if (issued < nblk) {  // aborted: let copies in flight land
         for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-          mbar_wait_quiet(bar_full + 8 * (i % kStages), (i / kStages) & 1, 500000000ull);
+          if (!(p.withhold_copy && i == 0))
+            mbar_wait_quiet(bar_full + 8 * (i % kStages), (i / kStages) & 1, 500000000ull);
       }
     }
     __syncthreads();  // pairs with the consumers' merge barrier below
@@ -197,7 +204,8 @@ __global__ void __launch_bounds__(kThreads)
 
   for (int i = warp; i < nblk; i += kConsumerWarps) {
     const int s = i % kStages;
-    if (!mbar_wait(bar_full + 8 * s, (i / kStages) & 1, abort, p.flags)) break;
+    if (!mbar_wait_warp(bar_full + 8 * s, (i / kStages) & 1, abort, p.flags, p.wait_limit_ns))
+      break;
     const uint32_t kbase = sbase + s * C::STAGE_BYTES;
     const uint32_t vbase = kbase + C::BLK_BYTES;
     const int n_valid = min(kBS, n_tok - i * kBS);

@@ -23,8 +23,9 @@ enum : unsigned {
 // its address as a parameter so no relocatable device code is needed.
 __device__ __forceinline__ void raise_flag(unsigned* flags, unsigned f) { atomicOr(flags, f); }
 
-// Wall-clock limit of any single wait (ns).  Kernels here run for milliseconds;
-// a wait this long means a broken pipeline, not a slow one.
+// Default wall-clock limit of any single wait (ns).  Kernels here run for
+// milliseconds; a wait this long means a broken pipeline, not a slow one.  The
+// limit actually used is a kernel parameter, so a test can shorten it.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -73,23 +74,68 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase with the given parity has completed.  Gives up (and
-// returns false) after kWaitLimitNs or as soon as *abort is set by another
+// try_wait that suspends the thread for at most hint_ns while the phase is
+// incomplete (it resumes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Suspension per poll: the wait limit, but at most 1 ms, so a limit is noticed
+// within about a millisecond of running out.
+__device__ __forceinline__ uint32_t poll_hint(unsigned long long limit_ns) {
+  return limit_ns < 1000000ull ? static_cast<uint32_t>(limit_ns) : 1000000u;
+}
+
+// Waits (one thread) until the phase with the given parity has completed.  Gives
+// up (and returns false) after limit_ns or as soon as *abort is set by another
 // role of the same CTA; on a timeout it raises DEVFLAG_TIMEOUT and sets *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned* flags) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                          unsigned* flags,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+  const uint32_t hint = poll_hint(limit_ns);
+  if (mbar_try_wait_hint(bar, parity, hint)) return true;
   const unsigned long long t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, hint)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      raise_flag(flags, DEVFLAG_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+// The same wait for a whole warp: every lane polls, and the result (and the
+// abort / timeout decision, taken by lane 0) is the same in every lane, so the
+// warp stays converged for the .sync.aligned instructions that follow.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               unsigned* flags, unsigned long long limit_ns) {
+  const uint32_t hint = poll_hint(limit_ns);
+  if (__all_sync(0xffffffffu, mbar_try_wait_hint(bar, parity, hint))) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_hint(bar, parity, hint))) return true;
+    int give_up = 0;
+    if ((threadIdx.x & 31) == 0) {
+      if (*abort) {
+        give_up = 1;
+      } else if (globaltimer() - t0 > limit_ns) {
         raise_flag(flags, DEVFLAG_TIMEOUT);
         *abort = 1;
-        return false;
+        give_up = 1;
       }
     }
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
   }
 }
 
@@ -220,6 +266,26 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// 32 lanes x 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // 32 lanes x 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -274,6 +340,50 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Register reallocation between warpgroups (every thread of the warpgroup runs
+// the same instruction).  The block is launched with a fixed total; the counts
+// used with these must add up to at most that total.
+template <int N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Largest of three floats (the three-input max of sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x for a pair of values, evaluated on the FMA pipe instead of the
+// special-function unit, for x <= 127 (softmax exponents here are <= 8); inputs
+// below -126 are clamped there.  Cody-Waite style range reduction (W. J. Cody
+// and W. Waite, "Software Manual for the Elementary Functions", 1980): x = n + f
+// with n = round(x) and f in [-1/2, 1/2]; adding 1.5 * 2^23 rounds x to an
+// integer in the low mantissa bits, which also yields n << 23 as an integer.
+// 2^f is a degree-3 polynomial whose coefficients come from a minimax fit on
+// [-1/2, 1/2] (Lawson's iteratively reweighted least squares, evaluated in
+// fp32): max relative error 7.5e-5, far below the 2^-9 relative rounding of the
+// bf16 probabilities it produces.  The arithmetic uses the packed fp32x2 forms.
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+  const float2 kRound = make_float2(12582912.0f, 12582912.0f);  // 1.5 * 2^23
+  const float2 kMinus = make_float2(-12582912.0f, -12582912.0f);
+  const float2 xc = make_float2(fmaxf(x.x, -126.0f), fmaxf(x.y, -126.0f));
+  const float2 t = __fadd2_rn(xc, kRound);
+  const float2 n = __fadd2_rn(t, kMinus);
+  const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), xc);
+  float2 p = __ffma2_rn(make_float2(0.05517149344086647f, 0.05517149344086647f), f,
+                        make_float2(0.24261093139648438f, 0.24261093139648438f));
+  p = __ffma2_rn(p, f, make_float2(0.6932609677314758f, 0.6932609677314758f));
+  p = __ffma2_rn(p, f, make_float2(0.9999280571937561f, 0.9999280571937561f));
+  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -71,8 +71,42 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              int Hkv, int T, int D, int causal, float scale, void *stream);
 
 /*
+ * paged_attn_prefill -- attention of a chunk of new tokens against a paged KV
+ * cache (chunked prefill).  The blockwise computation of attn_fwd, with every key
+ * and value position translated through the block table (same the-ai.news
+ * section; block_size = 16 as in its vLLM example).
+ *
+ *   q             [B, Hq, Tq, D] bf16: the Tq newest tokens of each batch item
+ *   k_pool/v_pool [num_pool_blocks, Hkv, block_size, D] bf16
+ *   block_table   [B, max_blocks_per_seq] int32: logical block t / block_size of
+ *                 item b lives in physical block block_table[b][t / block_size];
+ *                 entries past ceil(kv_lens[b] / block_size) are never read
+ *   kv_lens       [B] int32 (device memory): tokens in each item's cache, the Tq
+ *                 new tokens' own keys and values included
+ *   o             [B, Hq, Tq, D] bf16 (written)
+ *   lse           [B, Hq, Tq] fp32 (written; may be NULL)
+ *
+ * Query i of item b is the token at logical position kv_lens[b] - Tq + i.  With
+ * causal != 0 it sees keys 0 .. kv_lens[b] - Tq + i (the mask is aligned with the
+ * last key); otherwise all kv_lens[b] keys.  A query that sees no key (causal
+ * with kv_lens[b] < Tq) gets O = 0 and LSE = -inf.  max_kv_len bounds every
+ * kv_lens[b].  block_size must be 16 and D 64 or 128.  Per-item data is checked
+ * on the device: a kv_lens[b] outside [0, min(max_kv_len, max_blocks_per_seq *
+ * block_size)] makes that item's O and LSE NaN and sets flag bit 2; a block id
+ * outside [0, num_pool_blocks) is read as block 0 and sets flag bit 4 (that
+ * item's output is then unspecified).  Pool slots past kv_lens[b] may hold any
+ * bits, NaN included: they never reach the output.
+ */
+int paged_attn_prefill(const void *q, const void *k_pool, const void *v_pool,
+                       const int32_t *block_table, const int32_t *kv_lens, int block_size, int B,
+                       int Hq, int Hkv, int Tq, int D, int max_blocks_per_seq,
+                       int num_pool_blocks, int max_kv_len, int causal, float scale, void *o,
+                       float *lse, void *stream);
+
+/*
  * Bytes of scratch workspace paged_attn_decode needs for these sizes (partial
- * outputs of the split-KV pass).  Depends only on the arguments.
+ * outputs of the split-KV pass).  Depends only on the arguments; the block size
+ * is not one of them (it is fixed at 16 and checked by paged_attn_decode).
  */
 size_t paged_attn_decode_workspace_size(int num_seqs, int Hq, int D, int max_seq_len);
 
@@ -145,13 +179,75 @@ int paged_attn_decode_noalloc(const void *q, const void *k_pool, const void *v_p
                               float *lse, void *stream);
 
 /*
- * Synchronises the current device, then reads and clears the library's device
- * flag word.  *flags (if not NULL) receives the raw bits: 1 = a bounded wait in
+ * Synchronises the current device (every stream), then reads and clears the
+ * library's device flag word.  The word is one per device, shared by every
+ * stream and every caller of the library in the process: a flag raised by any
+ * kernel of this library on that device stays set until the next call of this
+ * function, which reports and clears it for everyone.  *flags (if not NULL) receives the raw bits: 1 = a bounded wait in
  * a kernel timed out, 2 = a decode request had an invalid length, 4 = a decode
  * block id was out of range.  Returns ATTN_ERR_DEVICE if any bit was set,
  * ATTN_ERR_CUDA if the synchronisation failed, else ATTN_OK.
  */
 int attn_device_status(unsigned int *flags);
+
+/*
+ * paged_kv_append -- writes Tn new tokens per request into the paged KV cache (the
+ * cache "grows one token at a time", same the-ai.news section).
+ *
+ *   k_new, v_new  [num_seqs, Hkv, Tn, D] bf16: the new tokens' keys and values
+ *   k_pool/v_pool [num_pool_blocks, Hkv, block_size, D] bf16 (written in place)
+ *   block_table   [num_seqs, max_blocks_per_seq] int32; the blocks that the new
+ *                 positions fall into must already be assigned
+ *   seq_lens      [num_seqs] int32 (device): tokens already cached, L_r
+ *   new_seq_lens  [num_seqs] int32 (device, may be NULL): receives L_r + Tn; it
+ *                 must not overlap seq_lens
+ *
+ * Token t of request r goes to logical position L_r + t, i.e. physical block
+ * block_table[r][(L_r + t) / 16], slot (L_r + t) % 16.  The copy is exact (bits
+ * in = bits out).  Device-side checks: L_r < 0 or L_r + Tn > max_blocks_per_seq *
+ * block_size skips the request, sets flag bit 2 and writes L_r unchanged to
+ * new_seq_lens; a block id outside the pool skips that token and sets flag bit 4.
+ * block_size must be 16, D 64 or 128.
+ */
+int paged_kv_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool,
+                    const int32_t *block_table, const int32_t *seq_lens, int32_t *new_seq_lens,
+                    int block_size, int num_seqs, int Hkv, int Tn, int D, int max_blocks_per_seq,
+                    int num_pool_blocks, void *stream);
+
+/*
+ * paged_kv_gather -- copies each request's cached keys (or values) out of the
+ * paged pool in logical order, with the same block-table translation and the
+ * same TMA box copies that the attention kernels use.
+ *
+ *   pool          [num_pool_blocks, Hkv, block_size, D] bf16
+ *   block_table   [num_seqs, max_blocks_per_seq] int32
+ *   seq_lens      [num_seqs] int32 (device)
+ *   out           [num_seqs, Hkv, max_seq_len, D] bf16: out[r][h][t] = the row of
+ *                 token t < seq_lens[r]; rows t >= seq_lens[r] are not written
+ *
+ * Device-side checks: a length outside [0, min(max_seq_len, max_blocks_per_seq
+ * * block_size)] skips the request and sets flag bit 2; a block id outside the
+ * pool writes NaN rows for that block and sets flag bit 4.
+ */
+int paged_kv_gather(const void *pool, const int32_t *block_table, const int32_t *seq_lens,
+                    int block_size, int num_seqs, int Hkv, int D, int max_blocks_per_seq,
+                    int num_pool_blocks, int max_seq_len, void *out, void *stream);
+
+/*
+ * Test hook for the kernels' failure detection (not for production use).
+ * Kernels launched after this call use wait_limit_ns as the limit, in
+ * nanoseconds, of every pipeline wait (0 restores the default of 2 s).  With
+ * withhold_copy = 1 the copy warp of every CTA of the next kernels skips its
+ * first data copy, so a consumer's wait for it is certain to run out: the
+ * waiting role raises flag bit 1, tells the CTA's other roles to stop, lets the
+ * copies and MMAs already in flight finish, and the kernel returns with
+ * unspecified outputs; attn_device_status() then reports ATTN_ERR_DEVICE.  No
+ * fault, trap or hang is involved.  Call attn_test_set_failure(0, 0) to restore
+ * normal operation.  Process-wide; not meant for use while other threads launch
+ * kernels of this library.  Returns ATTN_OK, or ATTN_ERR_INVALID_ARG if
+ * withhold_copy is not 0 or 1.
+ */
+int attn_test_set_failure(unsigned long long wait_limit_ns, int withhold_copy);
 
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 int attn_version(void);

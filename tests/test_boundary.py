@@ -20,7 +20,8 @@ def declared_functions():
     with open(HEADER) as fh:
         text = fh.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+    pat = r"^\s*(?:const\s+)?(?:unsigned\s+)?(?:long\s+)*\w+(?:\s+|\s*\*\s*)(\w+)\s*\("
+    return sorted(set(re.findall(pat, text, flags=re.M)))
 
 
 @pytest.fixture(scope="module")
