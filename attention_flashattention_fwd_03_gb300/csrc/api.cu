@@ -323,7 +323,8 @@ GBATTN_API int paged_attn_decode(const void* q, const void* k_pool, const void* 
   p.flags = ds->flags;
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.withhold_copy = g_withhold_copy.load(std::memory_order_relaxed);
-  if (launch_paged_decode(tmK, tmV, p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (launch_paged_decode(tmK, tmV, p, ds->num_sms, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
 }

@@ -39,11 +39,13 @@
 #include "internal.h"
 #include "ptx.cuh"
 
-// One key pair in every GBATTN_EXP2_POLY_PAIRS of an unmasked tile has its
-// probabilities computed on the FMA pipe (exp2_fma2) instead of the
-// special-function unit, to balance the two pipes; 0 disables it.
+// With GBATTN_EXP2_POLY_PAIRS = n > 0, one key pair in every n of an unmasked
+// tile has its probabilities computed on the FMA pipe (exp2_fma2) instead of
+// the special-function unit.  Measured on GB300 the kernel is limited by issue
+// slots and latency rather than by the special-function unit, and every setting
+// tried (n = 2, 3, 4) was slower than 0, so it is off by default.
 #ifndef GBATTN_EXP2_POLY_PAIRS
-#define GBATTN_EXP2_POLY_PAIRS 4
+#define GBATTN_EXP2_POLY_PAIRS 0
 #endif
 
 namespace gbattn {

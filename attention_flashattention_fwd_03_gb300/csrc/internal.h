@@ -65,7 +65,7 @@ constexpr int kDecodeChunk = 512;  // logical tokens per split (fixed: results d
 // Paged decode.  tmK/tmV are 2-D tiled maps over the pools viewed as
 // [num_pool_blocks * Hkv * block_size, D] bf16 with a 64 x 16 box, 128-byte swizzle.
 cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                const DecodeParams& p, cudaStream_t stream);
+                                const DecodeParams& p, int num_sms, cudaStream_t stream);
 cudaError_t prepare_paged_decode();
 
 size_t decode_workspace_bytes(int S, int Hq, int D, int max_seq_len);

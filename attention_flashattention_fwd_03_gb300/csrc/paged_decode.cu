@@ -7,7 +7,9 @@
 // kernel translates every position through that table.
 //
 // GB300 realisation (HBM-bound: every K/V byte is read exactly once):
-//   split kernel   one CTA per (request, KV head, 512-token chunk).  A producer
+//   split kernel   one CTA per (request, KV head, 512-token chunk), three
+//                  resident per SM, chunks ordered chunk-index first so that the
+//                  CTAs of chunks past a request's end come last.  A producer
 //                  warp reads the chunk's (at most 32) block-table entries once,
 //                  then TMA-gathers each (physical block, KV head) slice -- 16
 //                  contiguous rows of D bf16 -- for K and V into an 8-stage,
@@ -21,22 +23,26 @@
 //                  workspace.
 //   merge kernel   one warp per (request, query head): LSE = M + ln sum_s
 //                  e^{LSE_s - M}, O = sum_s e^{LSE_s - LSE} O_s, in split order.
+//                  It is launched as a programmatic dependent of the split
+//                  kernel, so its launch overlaps the split kernel's tail.
 // The reduction order depends only on logical positions (fixed chunk length,
 // fixed block-to-warp assignment), so any placement of the blocks in the pool
 // gives bit-identical results.
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "paged.cuh"
 #include "ptx.cuh"
 
 namespace gbattn {
 
 namespace {
 
-constexpr int kBS = 16;          // tokens per KV block
+constexpr int kBS = kPagedBlock;  // tokens per KV block
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 8;
+constexpr int kCtasPerSm = 3;  // 3 x 66 KB of shared memory, <= 136 registers per thread
 constexpr int kBlocksPerChunk = kDecodeChunk / kBS;  // 32
 
 template <int D>
@@ -89,7 +95,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int col) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                               const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
   using C = DecCfg<D>;
@@ -103,9 +109,13 @@ __global__ void __launch_bounds__(kThreads)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
   volatile int* bad = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
+  // the merge kernel may be scheduled now; it waits for this grid's results
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x % p.max_splits;
-  const int rk = blockIdx.x / p.max_splits;
+  const int n_rk = p.S * p.Hkv;
+  const int split = blockIdx.x / n_rk;  // chunk index first: empty chunks come last
+  const int rk = blockIdx.x - split * n_rk;
   const int kvh = rk % p.Hkv;
   const int r = rk / p.Hkv;
   const int L = p.seq_lens[r];
@@ -129,15 +139,15 @@ __global__ void __launch_bounds__(kThreads)
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
-    int phys = 0;
     if (lane < nblk) {
-      phys = p.block_table[static_cast<size_t>(r) * p.max_blocks + c0 / kBS + lane];
-      if (phys < 0 || phys >= p.num_pool_blocks) {
+      int row = paged_block_row(p.block_table, p.max_blocks, r, c0 / kBS + lane, kvh, p.Hkv,
+                                p.num_pool_blocks);
+      if (row < 0) {
         raise_flag(p.flags, DEVFLAG_BAD_BLOCK);
         *bad = 1;
-        phys = 0;
+        row = kvh * kBS;  // read block 0 instead; the chunk is reported as NaN
       }
-      table[lane] = phys;
+      table[lane] = row;
     }
     __syncwarp();
     if (lane == 0) {
@@ -148,7 +158,7 @@ __global__ void __launch_bounds__(kThreads)
                        p.wait_limit_ns))
           break;
         const uint32_t dst = sbase + s * C::STAGE_BYTES;
-        const int row = (table[i] * p.Hkv + kvh) * kBS;
+        const int row = table[i];
         if (p.withhold_copy && i == 0) {  // test hook: the first block never arrives
           ++issued;
           continue;
@@ -347,6 +357,9 @@ __global__ void __launch_bounds__(kThreads)
 template <int D>
 __global__ void __launch_bounds__(128)
     paged_decode_merge_kernel(const DecodeParams p) {
+  // launched as a programmatic dependent: the split kernel's results are complete
+  // and visible once this returns
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp_global >= p.S * p.Hq) return;
@@ -423,20 +436,35 @@ cudaError_t prepare_paged_decode() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<128>::SMEM_BYTES);
 }
 
-cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                const DecodeParams& p, cudaStream_t stream) {
-  if (p.S <= 0) return cudaSuccess;
+namespace {
+
+template <int D>
+cudaError_t launch_pair(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p,
+                        cudaStream_t stream) {
   const int grid = p.S * p.Hkv * p.max_splits;
-  const int merge_blocks = (p.S * p.Hq + 3) / 4;
-  if (p.D == 64) {
-    paged_decode_split_kernel<64><<<grid, kThreads, DecCfg<64>::SMEM_BYTES, stream>>>(tmK, tmV, p);
-    paged_decode_merge_kernel<64><<<merge_blocks, 128, 0, stream>>>(p);
-  } else {
-    paged_decode_split_kernel<128>
-        <<<grid, kThreads, DecCfg<128>::SMEM_BYTES, stream>>>(tmK, tmV, p);
-    paged_decode_merge_kernel<128><<<merge_blocks, 128, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  paged_decode_split_kernel<D><<<grid, kThreads, DecCfg<D>::SMEM_BYTES, stream>>>(tmK, tmV, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.S * p.Hq + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel<D>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                const DecodeParams& p, int num_sms, cudaStream_t stream) {
+  (void)num_sms;
+  if (p.S <= 0) return cudaSuccess;
+  return p.D == 64 ? launch_pair<64>(tmK, tmV, p, stream) : launch_pair<128>(tmK, tmV, p, stream);
 }
 
 }  // namespace gbattn
