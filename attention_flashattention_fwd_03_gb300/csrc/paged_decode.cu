@@ -380,24 +380,37 @@ __global__ void __launch_bounds__(128)
     for (int i = 0; i < PER; ++i) res[i] = 0.f;
     lse_out = -INFINITY;
   } else {
+    // All partial LSEs are loaded at once (one lane each), reduced across the
+    // warp, and the partial outputs are then read with every load in flight, so
+    // the merge costs a couple of memory round trips, not one per split.
     const int ns = (L + kDecodeChunk - 1) / kDecodeChunk;
     const float* pl = p.part_lse + hq * p.max_splits;
+    const float* po = p.part_o + hq * p.max_splits * D + lane * PER;
     float M = -INFINITY;
     bool nan = false;
-    for (int s = 0; s < ns; ++s) {
-      const float v = pl[s];
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      const float v = (s0 + lane < ns) ? pl[s0 + lane] : -INFINITY;
       nan |= (v != v);
       M = fmaxf(M, v);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    nan = __any_sync(0xffffffffu, nan);
     float tot = 0.f;
 #pragma unroll
     for (int i = 0; i < PER; ++i) res[i] = 0.f;
-    const float* po = p.part_o + hq * p.max_splits * D + lane * PER;
-    for (int s = 0; s < ns; ++s) {
-      const float w = __expf(pl[s] - M);
-      tot += w;
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      const int n = min(32, ns - s0);
+      const float w_lane = (lane < n) ? __expf(pl[s0 + lane] - M) : 0.f;
+      // in split order: lane s holds the weight of split s0 + s
+#pragma unroll 4
+      for (int s = 0; s < n; ++s) {
+        const float w = __shfl_sync(0xffffffffu, w_lane, s);
+        tot += w;
+        const float* src = po + static_cast<size_t>(s0 + s) * D;
 #pragma unroll
-      for (int i = 0; i < PER; ++i) res[i] += w * po[static_cast<size_t>(s) * D + i];
+        for (int i = 0; i < PER; ++i) res[i] += w * src[i];
+      }
     }
     const float inv = 1.f / tot;
 #pragma unroll

@@ -47,6 +47,11 @@ METRIC = "attn fwd TFLOP/s & % bf16 tensor peak; paged-decode KV GB/s & % HBM pe
 HEADLINE = synth.CONFIGS["prefill_gqa_long_causal"]
 DECODE = synth.CONFIGS["paged_decode"]
 OTHER_PREFILL = [synth.CONFIGS[n] for n in ("tiny_causal", "prefill_mha_causal", "noncausal_d64")]
+# chunked prefill against the paged cache: 16 sequences, 512 new tokens each,
+# cache lengths U[1024, 8192] (the chunk included), GQA 32/8, D=128, causal
+CHUNKED = synth.DecodeConfig("chunked_prefill", 16, 32, 8, 128, 1024, 8192, 16, 6000)
+CHUNK_TQ = 512
+NAIVE = synth.CONFIGS["prefill_mha_causal"]
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -212,6 +217,13 @@ def aggregate_value(flops_per_rank: float, ms_max: float, world: int) -> float:
     return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
+def chunked_flops(kv_lens, Tq, Hq, D) -> float:
+    """q.k and p.v multiply-adds of causal chunks: query i of an item with L keys
+    sees L - Tq + i + 1 keys."""
+    pairs = sum(Tq * (int(L) - Tq) + Tq * (Tq + 1) / 2 for L in kv_lens)
+    return 4.0 * Hq * D * pairs
+
+
 def decode_bytes(pg, cfg) -> int:
     """Algorithmic bytes of one decode launch: K/V of every cached token plus q, o, lse,
     the block-table entries in use and seq_lens."""
@@ -335,6 +347,80 @@ def run_ours(args, rank, world, local_rank):
         del bufs, call
     R.check_status("after the other workloads")
 
+    # ---- chunked prefill through the block table ----
+    pc = synth.paged_inputs(CHUNKED)
+    qc = R.to_dev(synth.normal_bf16(CHUNKED.seed + 9, (CHUNKED.num_seqs, CHUNKED.Hq, CHUNK_TQ,
+                                                       CHUNKED.D)))
+    kpc, vpc = R.to_dev(pc.k_pool), R.to_dev(pc.v_pool)
+    btc, klc = R.i32(pc.block_table), R.i32(pc.seq_lens)
+    oc = torch.empty_like(qc)
+    lc = torch.empty(qc.shape[:3], dtype=torch.float32, device=dev)
+
+    def chunked_call():
+        gb.paged_attn_prefill(qc, kpc, vpc, btc, klc, pc.max_seq_len, causal=True,
+                              scale=CHUNKED.softmax_scale, out=oc, lse=lc)
+    (t_chunk,) = R.time_calls([chunked_call], args.steps, 3)
+    chunk_flops = chunked_flops(pc.seq_lens, CHUNK_TQ, CHUNKED.Hq, CHUNKED.D)
+    del qc, kpc, vpc, oc, lc
+
+    # ---- one decode step (append the new token, then decode), eager vs graph ----
+    pa = synth.paged_inputs(DECODE, seq_lens=pg.seq_lens + 1, max_seq_len=pg.max_seq_len + 1)
+    ka, va = R.to_dev(pa.k_pool), R.to_dev(pa.v_pool)
+    bta = R.i32(pa.block_table)
+    lens_before = R.i32(pg.seq_lens)
+    lens_after = torch.empty_like(lens_before)
+    qa = R.to_dev(pg.q)
+    k_new = R.to_dev(synth.normal_bf16(DECODE.seed + 21, (DECODE.num_seqs, DECODE.Hkv, 1,
+                                                           DECODE.D)))
+    v_new = R.to_dev(synth.normal_bf16(DECODE.seed + 22, (DECODE.num_seqs, DECODE.Hkv, 1,
+                                                           DECODE.D)))
+    oa = torch.empty_like(qa)
+    la = torch.empty((DECODE.num_seqs, DECODE.Hq), dtype=torch.float32, device=dev)
+    wsa = torch.empty(gb.paged_attn_decode_workspace_size(DECODE.num_seqs, DECODE.Hq, DECODE.D,
+                                                          pa.max_seq_len), dtype=torch.uint8,
+                      device=dev)
+
+    def decode_step():
+        gb.paged_kv_append(k_new, v_new, ka, va, bta, lens_before, lens_after)
+        gb.paged_attn_decode(qa, ka, va, bta, lens_after, pa.max_seq_len,
+                             scale=DECODE.softmax_scale, out=oa, lse=la, workspace=wsa)
+    for _ in range(3):
+        decode_step()
+    torch.cuda.synchronize()
+    n_rep = 200
+
+    def time_loop(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(R.stream)
+        for _ in range(n_rep):
+            fn()
+        e1.record(R.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n_rep
+    us_eager = time_loop(decode_step)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(R.stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        decode_step()
+    torch.cuda.synchronize()
+    us_graph = time_loop(graph.replay)
+    R.check_status("after the decode-step loop")
+    del graph, ka, va, wsa
+
+    # ---- the naive unfused sequence (matmul, scale, mask, softmax, matmul) ----
+    nq, nk, nv = (R.to_dev(x) for x in synth.prefill_inputs(NAIVE))
+    mask = torch.ones(NAIVE.T, NAIVE.T, dtype=torch.bool, device=dev).triu(1)
+
+    def naive_call():
+        s_ = torch.matmul(nq, nk.transpose(-1, -2))
+        s_ = s_ * NAIVE.softmax_scale
+        s_ = s_.masked_fill(mask, float("-inf"))
+        p_ = torch.softmax(s_, dim=-1)
+        return torch.matmul(p_, nv)
+    (t_naive,) = R.time_calls([naive_call], max(3, args.steps // 2), 2)
+    del nq, nk, nv, mask
+
     # ---- e2e: host buffers, copies inside the timed region ----
     q, k, v, o, lse = pre_bufs
     pin = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()  # noqa: E731
@@ -355,8 +441,9 @@ def run_ours(args, rank, world, local_rank):
     d2h = ho.numel() * 2 + hl.numel() * 4
 
     # ---- aggregate over ranks (max of medians) ----
-    names = ["pre", "dec", "e2e"] + list(other)
-    meds = [stats(t_pre)["median"], stats(t_dec)["median"], stats(t_e2e)["median"]] + \
+    names = ["pre", "dec", "e2e", "chunk", "naive"] + list(other)
+    meds = [stats(t_pre)["median"], stats(t_dec)["median"], stats(t_e2e)["median"],
+            stats(t_chunk)["median"], stats(t_naive)["median"]] + \
         [stats(other[n])["median"] for n in other]
     meds_max = max_over_ranks(meds + [wall], dev)
     med = dict(zip(names, meds_max[:-1]))
@@ -373,6 +460,8 @@ def run_ours(args, rank, world, local_rank):
                "paged_decode": {"value": gbs, "unit": "GB/s", "cores": dcores, "kind": "oracle",
                                 "sample": f"the whole paged decode workload in {dsec:.2f} s"}}
     return dict(med=med, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e, other=other,
+                t_chunk=t_chunk, chunk_flops=chunk_flops, us_eager=us_eager, us_graph=us_graph,
+                t_naive=t_naive,
                 wall=meds_max[-1], clocks=clocks, launches=args.steps * 3,
                 h2d=h2d, d2h=d2h, cpu=cpu, dec_bytes=decode_bytes(pg, DECODE),
                 kv_bytes=pg.kv_bytes(DECODE.Hkv, DECODE.D))
@@ -399,6 +488,7 @@ def report_ours(args, res, world):
     gbs = res["dec_bytes"] / (med["dec"] * 1e-3) / 1e9
     e2e_tf = world * flops / (med["e2e"] * 1e-3) / 1e12
     kname = f"attn_fwd_kernel<{HEADLINE.D}>"
+    naive_ours_ms = med[NAIVE.name]
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -454,6 +544,25 @@ def report_ours(args, res, world):
                          "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "traffic": load_traffic(f"paged_decode {DECODE.name}")},
         },
+        "paged_prefill": {
+            "workload": (f"chunked prefill: {CHUNKED.num_seqs} sequences x {CHUNK_TQ} new tokens, "
+                         f"cache lengths U[{CHUNKED.len_lo},{CHUNKED.len_hi}], Hq={CHUNKED.Hq} "
+                         f"Hkv={CHUNKED.Hkv} D={CHUNKED.D}, causal, block_size 16"),
+            "tflops": round(res["chunk_flops"] / (med["chunk"] * 1e-3) / 1e12, 2),
+            "frac": round(res["chunk_flops"] / (med["chunk"] * 1e-3) / 1e12
+                          / peaks["bf16_tflops"], 4),
+            "flops": res["chunk_flops"], "flop_convention": "exact visible (query, key) pairs",
+            "ms": {k: round(v, 5) for k, v in stats(res["t_chunk"]).items()}},
+        "decode_step": {
+            "what": "paged_kv_append of one token per request + paged_attn_decode, decode workload",
+            "us_eager": round(res["us_eager"], 2), "us_cuda_graph": round(res["us_graph"], 2),
+            "launches_per_step": 3},
+        "naive_unfused": {
+            "what": (f"torch matmul, scale, masked_fill, softmax, matmul on {NAIVE.name} "
+                     "(context only; not a product path)"),
+            "ms": round(med["naive"], 4),
+            "tflops": round(NAIVE.flops() / (med["naive"] * 1e-3) / 1e12, 2),
+            "speedup_of_attn_fwd": round(med["naive"] / naive_ours_ms, 2)},
         "e2e": {"value": round(e2e_tf, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "ms_per_step": round(med["e2e"], 4),
@@ -478,6 +587,19 @@ def run_single(args, local_rank):
         pg = synth.paged_inputs(DECODE)
         call = R.decode_call(DECODE, pg)
         work, unit = decode_bytes(pg, DECODE) / 1e9, "GB/s"
+    elif name == CHUNKED.name:
+        import attention_flashattention_fwd_03_gb300 as gb
+        import torch
+        pc = synth.paged_inputs(CHUNKED)
+        qc = R.to_dev(synth.normal_bf16(CHUNKED.seed + 9, (CHUNKED.num_seqs, CHUNKED.Hq, CHUNK_TQ,
+                                                           CHUNKED.D)))
+        kpc, vpc = R.to_dev(pc.k_pool), R.to_dev(pc.v_pool)
+        btc, klc = R.i32(pc.block_table), R.i32(pc.seq_lens)
+
+        def call():
+            gb.paged_attn_prefill(qc, kpc, vpc, btc, klc, pc.max_seq_len, causal=True,
+                                  scale=CHUNKED.softmax_scale)
+        work, unit = chunked_flops(pc.seq_lens, CHUNK_TQ, CHUNKED.Hq, CHUNKED.D) / 1e12, "TFLOP/s"
     else:
         cfg = synth.CONFIGS[name]
         call, _bufs = R.prefill_call(cfg)
@@ -535,7 +657,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(synth.CONFIGS), default=None)
+    ap.add_argument("--workload", choices=sorted(synth.CONFIGS) + [CHUNKED.name], default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
