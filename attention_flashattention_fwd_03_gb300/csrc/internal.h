@@ -60,7 +60,10 @@ struct DecodeParams {
   int withhold_copy;           // test hook: the producer skips its first copy
 };
 
-constexpr int kDecodeChunk = 512;  // logical tokens per split (fixed: results depend only on logical positions)
+#ifndef GBATTN_DEC_CHUNK
+#define GBATTN_DEC_CHUNK 512
+#endif
+constexpr int kDecodeChunk = GBATTN_DEC_CHUNK;  // logical tokens per split (fixed: results depend only on logical positions)
 
 // Paged decode.  tmK/tmV are 2-D tiled maps over the pools viewed as
 // [num_pool_blocks * Hkv * block_size, D] bf16 with a 64 x 16 box, 128-byte swizzle.

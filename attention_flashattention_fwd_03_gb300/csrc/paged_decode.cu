@@ -41,8 +41,21 @@ namespace {
 constexpr int kBS = kPagedBlock;  // tokens per KV block
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 8;
-constexpr int kCtasPerSm = 3;  // 3 x 66 KB of shared memory, <= 136 registers per thread
+#ifndef GBATTN_DEC_STAGES
+#define GBATTN_DEC_STAGES 8
+#endif
+#ifndef GBATTN_DEC_CTAS_PER_SM
+#define GBATTN_DEC_CTAS_PER_SM 3
+#endif
+constexpr int kStages = GBATTN_DEC_STAGES;          // 8 KiB K+V stages per CTA
+constexpr int kCtasPerSm = GBATTN_DEC_CTAS_PER_SM;  // 3 x 66 KB of shared memory, <= 136 registers
+// Block i goes to stage i % kStages and to consumer warp i % kConsumerWarps.  A
+// stage must always come back to the same warp: that warp then sees every phase
+// of the stage's barrier in order.  If two warps shared a stage across phases, a
+// warp could wait on a phase two behind (copies may land out of order), pass the
+// parity test early, read a stage that is still being written and break the
+// barrier's arrival and transaction counts.
+static_assert(kStages % kConsumerWarps == 0, "every stage must belong to one consumer warp");
 constexpr int kBlocksPerChunk = kDecodeChunk / kBS;  // 32
 
 template <int D>
@@ -139,15 +152,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
-    if (lane < nblk) {
-      int row = paged_block_row(p.block_table, p.max_blocks, r, c0 / kBS + lane, kvh, p.Hkv,
+    for (int b = lane; b < nblk; b += 32) {
+      int row = paged_block_row(p.block_table, p.max_blocks, r, c0 / kBS + b, kvh, p.Hkv,
                                 p.num_pool_blocks);
       if (row < 0) {
         raise_flag(p.flags, DEVFLAG_BAD_BLOCK);
         *bad = 1;
         row = kvh * kBS;  // read block 0 instead; the chunk is reported as NaN
       }
-      table[lane] = row;
+      table[b] = row;
     }
     __syncwarp();
     if (lane == 0) {
@@ -380,15 +393,22 @@ __global__ void __launch_bounds__(128)
     for (int i = 0; i < PER; ++i) res[i] = 0.f;
     lse_out = -INFINITY;
   } else {
-    // All partial LSEs are loaded at once (one lane each), reduced across the
-    // warp, and the partial outputs are then read with every load in flight, so
-    // the merge costs a couple of memory round trips, not one per split.
+    // The LSE of split `lane` and the partial outputs of the first 16 splits are
+    // loaded together, so the merge costs one memory round trip after the
+    // length; longer sequences (> 16 splits) read the rest in a second pass.
+    constexpr int kHeld = 16;
     const int ns = (L + kDecodeChunk - 1) / kDecodeChunk;
     const float* pl = p.part_lse + hq * p.max_splits;
     const float* po = p.part_o + hq * p.max_splits * D + lane * PER;
-    float M = -INFINITY;
-    bool nan = false;
-    for (int s0 = 0; s0 < ns; s0 += 32) {
+    const float lse_lane = (lane < ns) ? pl[lane] : -INFINITY;
+    float part[kHeld][PER];
+#pragma unroll
+    for (int s = 0; s < kHeld; ++s)
+#pragma unroll
+      for (int q = 0; q < PER; ++q) part[s][q] = (s < ns) ? po[static_cast<size_t>(s) * D + q] : 0.f;
+    float M = lse_lane;
+    bool nan = (lse_lane != lse_lane);
+    for (int s0 = 32; s0 < ns; s0 += 32) {
       const float v = (s0 + lane < ns) ? pl[s0 + lane] : -INFINITY;
       nan |= (v != v);
       M = fmaxf(M, v);
@@ -396,15 +416,22 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     nan = __any_sync(0xffffffffu, nan);
+    // weights and sums in split order
     float tot = 0.f;
 #pragma unroll
     for (int i = 0; i < PER; ++i) res[i] = 0.f;
+    const float w_first = (lane < ns) ? __expf(lse_lane - M) : 0.f;
+#pragma unroll
+    for (int s = 0; s < kHeld; ++s) {
+      const float w = __shfl_sync(0xffffffffu, w_first, s);  // 0 past ns
+      tot += w;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) res[i] += w * part[s][i];
+    }
     for (int s0 = 0; s0 < ns; s0 += 32) {
-      const int n = min(32, ns - s0);
-      const float w_lane = (lane < n) ? __expf(pl[s0 + lane] - M) : 0.f;
-      // in split order: lane s holds the weight of split s0 + s
-#pragma unroll 4
-      for (int s = 0; s < n; ++s) {
+      const float w_lane =
+          (s0 + lane < ns) ? (s0 == 0 ? w_first : __expf(pl[s0 + lane] - M)) : 0.f;
+      for (int s = max(kHeld - s0, 0); s < min(32, ns - s0); ++s) {
         const float w = __shfl_sync(0xffffffffu, w_lane, s);
         tot += w;
         const float* src = po + static_cast<size_t>(s0 + s) * D;
