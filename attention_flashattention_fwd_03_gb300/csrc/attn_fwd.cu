@@ -263,19 +263,23 @@ __device__ void producer_warp(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 }
 
 // ---------------------------------------------------------------------------
-// MMA warp: lane 0 issues every tcgen05.mma; the whole warp waits (and, in
-// paged mode, clears key rows past the sequence end in the last V tile)
+// MMA warp: the whole warp runs this code, waits together and issues every
+// tcgen05.mma and commit from the one lane elect.sync picks (in paged mode it
+// also clears key rows past the sequence end in the last V tile).  Shared-memory
+// descriptors are built once; an MMA only adds constant offsets to them.
 // ---------------------------------------------------------------------------
 template <int D, bool PAGED>
 struct MmaWarp {
   using C = Cfg<D>;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);  // A (P) in TMEM, V MN-major
+  static constexpr uint64_t kTileStep = C::TILE_BYTES >> 4;  // descriptor address units
 
   const FwdParams& p;
   const Bars<D>& bar;
   volatile int* abort;
-  uint32_t sQ, sR, tmem;
+  uint32_t sR, tmem;
+  uint64_t dq, dk, dv;   // descriptors of Q tile 0 and of ring slot 0 read as K and as V
   int lane;
   int base = 0;          // ring index of the unit's K_0
   int n_pv[2] = {0, 0};  // P V products issued per query tile, all units
@@ -284,7 +288,10 @@ struct MmaWarp {
 
   __device__ MmaWarp(const FwdParams& p_, const Bars<D>& b_, volatile int* a_, uint32_t sbase,
                      uint32_t tmem_)
-      : p(p_), bar(b_), abort(a_), sQ(sbase + C::OFF_Q), sR(sbase + C::OFF_RING), tmem(tmem_),
+      : p(p_), bar(b_), abort(a_), sR(sbase + C::OFF_RING), tmem(tmem_),
+        dq(smem_desc_sw128(sbase + C::OFF_Q, 16, 1024)),
+        dk(smem_desc_sw128(sbase + C::OFF_RING, 16, 1024)),
+        dv(smem_desc_sw128(sbase + C::OFF_RING, C::BOX_BYTES, 1024)),
         lane(threadIdx.x & 31) {}
 
   __device__ bool wait(uint32_t b, uint32_t parity) {
@@ -293,40 +300,38 @@ struct MmaWarp {
   __device__ int slot(int idx) const { return (base + idx) % C::NSLOT; }
   __device__ uint32_t par(int idx) const { return ((base + idx) / C::NSLOT) & 1; }
 
-  // S_i = Q_i K_j^T.  It overwrites the TMEM columns that P_i of the previous
+  // S_I = Q_I K_j^T.  It overwrites the TMEM columns that P_I of the previous
   // tile occupies; the P V product reading them was issued earlier by this same
   // thread, and one thread's tcgen05.mma operations execute in issue order, so
-  // that product has read P_i before this one writes there.
-  __device__ bool issue_s(int i, int j) {
+  // that product has read P_I before this one writes there.
+  template <int I>
+  __device__ bool issue_s(int j) {
     const int ks = slot(2 * j);
     if (!wait(bar.slot_full(ks), par(2 * j))) return false;
     tc_fence_after();
-    if (lane == 0) {
-      const uint32_t q = sQ + i * C::TILE_BYTES, k = sR + ks * C::TILE_BYTES;
+    const uint64_t a = dq + I * kTileStep, b = dk + static_cast<uint64_t>(ks) * kTileStep;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-        mma_ss(tmem + C::s_col(i), smem_desc_sw128(q + off, 16, 1024),
-               smem_desc_sw128(k + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(bar.s_full(i));
-      if (s_left == 1) mma_commit(bar.q_empty());  // the unit's last read of Q
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = ((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4;
+      mma_ss_warp(tmem + C::s_col(I), a + off, b + off, kIdescQK, kk > 0 ? 1u : 0u);
     }
+    mma_commit_warp(bar.s_full(I));
+    if (s_left == 1) mma_commit_warp(bar.q_empty());  // the unit's last read of Q
     --s_left;
     return true;
   }
 
-  // O_i += P_i V_j (P_i from TMEM)
-  __device__ bool issue_pv(int i, int j, int nkv, int L) {
+  // O_I += P_I V_j (P_I from TMEM)
+  template <int I>
+  __device__ bool issue_pv(int j, int nkv, int L) {
     const int vs = slot(2 * j + 1);
     if (!wait(bar.slot_full(vs), par(2 * j + 1))) return false;
-    const uint32_t v = sR + vs * C::TILE_BYTES;
     if (PAGED && j == nkv - 1 && zeroed_j != j) {
       zeroed_j = j;
       // Key rows past the sequence end hold stale or arbitrary data (even NaN);
       // their probabilities are 0, but 0 * NaN would reach O.  Clear those rows.
       const int row0 = max(0, L - j * BN);
-      uint8_t* gv = reinterpret_cast<uint8_t*>(__cvta_shared_to_generic(v));
+      uint8_t* gv = reinterpret_cast<uint8_t*>(__cvta_shared_to_generic(sR + vs * C::TILE_BYTES));
       for (int e = row0 * 8 + lane; e < BN * 8; e += 32) {  // 8 x 16 bytes per 128-byte row
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb)
@@ -335,17 +340,15 @@ struct MmaWarp {
       fence_proxy_async_smem();
       __syncwarp();
     }
-    if (!wait(bar.p_full(i), n_pv[i] & 1)) return false;
+    if (!wait(bar.p_full(I), n_pv[I] & 1)) return false;
     tc_fence_after();
-    if (lane == 0) {
+    const uint64_t b = dv + static_cast<uint64_t>(vs) * kTileStep;
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
-        mma_ts(tmem + C::o_col(i), tmem + C::p_col(i) + 8 * kk,
-               smem_desc_sw128(v + kk * 16 * 128, C::BOX_BYTES, 1024), kIdescPV,
-               (j > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(bar.s_free(i));
-    }
-    ++n_pv[i];
+    for (int kk = 0; kk < BN / 16; ++kk)
+      mma_ts_warp(tmem + C::o_col(I), tmem + C::p_col(I) + 8 * kk, b + ((kk * 16 * 128) >> 4),
+                  kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+    mma_commit_warp(bar.s_free(I));
+    ++n_pv[I];
     return true;
   }
 
@@ -360,17 +363,17 @@ struct MmaWarp {
       const int n0 = U.n[0], n1 = U.n[1], nkv = U.nkv;
       s_left = n0 + n1;
       zeroed_j = -1;
-      if (s_left == 0 && lane == 0) mma_commit(bar.q_empty());
-      if (n0 > 0 && !issue_s(0, 0)) return;
-      if (n1 > 0 && !issue_s(1, 0)) return;
-      if (nkv > 0 && lane == 0) mma_commit(bar.slot_empty(slot(0)));
+      if (s_left == 0) mma_commit_warp(bar.q_empty());
+      if (n0 > 0 && !issue_s<0>(0)) return;
+      if (n1 > 0 && !issue_s<1>(0)) return;
+      if (nkv > 0) mma_commit_warp(bar.slot_empty(slot(0)));
       for (int j = 0; j < nkv; ++j) {
-        if (j < n0 && !issue_pv(0, j, nkv, U.L)) return;
-        if (j + 1 < n0 && !issue_s(0, j + 1)) return;
-        if (j < n1 && !issue_pv(1, j, nkv, U.L)) return;
-        if (lane == 0) mma_commit(bar.slot_empty(slot(2 * j + 1)));
-        if (j + 1 < n1 && !issue_s(1, j + 1)) return;
-        if (j + 1 < nkv && lane == 0) mma_commit(bar.slot_empty(slot(2 * j + 2)));
+        if (j < n0 && !issue_pv<0>(j, nkv, U.L)) return;
+        if (j + 1 < n0 && !issue_s<0>(j + 1)) return;
+        if (j < n1 && !issue_pv<1>(j, nkv, U.L)) return;
+        mma_commit_warp(bar.slot_empty(slot(2 * j + 1)));
+        if (j + 1 < n1 && !issue_s<1>(j + 1)) return;
+        if (j + 1 < nkv) mma_commit_warp(bar.slot_empty(slot(2 * j + 2)));
       }
       base += 2 * nkv;
     }
@@ -601,10 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       MmaWarp<D, PAGED> mma(p, bar, abort, sbase, tmem);
       mma.run();
       // Every MMA this warp issued has finished once the teardown barrier flips.
-      if (lane == 0) {
-        mma_commit(bar.teardown());
-        mbar_wait_quiet(bar.teardown(), 0, 1000000000ull);
-      }
+      mma_commit_warp(bar.teardown());
+      if (lane == 0) mbar_wait_quiet(bar.teardown(), 0, 1000000000ull);
       __syncwarp();
     }
   } else {
