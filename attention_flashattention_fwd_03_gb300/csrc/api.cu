@@ -278,9 +278,7 @@ GBATTN_API int paged_attn_decode(const void* q, const void* k_pool, const void* 
   const size_t need = decode_workspace_bytes(num_seqs, Hq, D, max_seq_len);
   if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
   const uint64_t rows = static_cast<uint64_t>(num_pool_blocks) * Hkv * block_size;
-  const int max_splits = (max_seq_len + kDecodeChunk - 1) / kDecodeChunk;
-  if (rows >= kMaxDim ||
-      static_cast<uint64_t>(num_seqs) * Hkv * (max_splits > 0 ? max_splits : 1) >= kMaxDim ||
+  if (rows >= kMaxDim || static_cast<uint64_t>(num_seqs) * Hq >= kMaxDim ||
       static_cast<uint64_t>(num_seqs) * max_blocks_per_seq >= (1ull << 40))
     return ATTN_ERR_UNSUPPORTED;
 
@@ -303,11 +301,12 @@ GBATTN_API int paged_attn_decode(const void* q, const void* k_pool, const void* 
   p.seq_lens = seq_lens;
   p.o = o;
   p.lse = lse;
-  const size_t splits = static_cast<size_t>(max_splits > 0 ? max_splits : 1);
-  const size_t n = static_cast<size_t>(num_seqs) * Hq * splits;
-  p.part_o = static_cast<float*>(workspace);
-  p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        ((n * D * sizeof(float) + 255) & ~static_cast<size_t>(255)));
+  const DecodeWorkspace wl = decode_workspace_layout(num_seqs, Hq, D, max_seq_len);
+  char* ws = static_cast<char*>(workspace);
+  p.part_o = reinterpret_cast<float*>(ws);
+  p.part_lse = reinterpret_cast<float*>(ws + wl.off_part_lse);
+  p.seg_first = reinterpret_cast<long long*>(ws + wl.off_seg_first);
+  p.plan = reinterpret_cast<long long*>(ws + wl.off_plan);
   p.S = num_seqs;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -317,7 +316,7 @@ GBATTN_API int paged_attn_decode(const void* q, const void* k_pool, const void* 
   p.max_blocks = max_blocks_per_seq;
   p.num_pool_blocks = num_pool_blocks;
   p.max_seq_len = max_seq_len;
-  p.max_splits = static_cast<int>(splits);
+  p.max_pieces = decode_max_pieces(max_seq_len);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.flags = ds->flags;

@@ -45,14 +45,16 @@ struct DecodeParams {
   const int32_t* seq_lens;     // [S]
   void* o;                     // [S, Hq, D] bf16
   float* lse;                  // [S, Hq] or nullptr
-  float* part_o;               // [S, Hq, max_splits, D] fp32 (workspace)
-  float* part_lse;             // [S, Hq, max_splits] fp32 (workspace)
+  float* part_o;               // [S, Hq, max_pieces, D] fp32 (workspace)
+  float* part_lse;             // [S, Hq, max_pieces] fp32 (workspace)
+  long long* seg_first;        // [S, Hkv] first global block of each segment (workspace)
+  long long* plan;             // [2]: total blocks NB, warp ranges W (workspace)
   int S, Hq, Hkv, D, group;
   int block_size;
   int max_blocks;
   int num_pool_blocks;
   int max_seq_len;
-  int max_splits;
+  int max_pieces;              // bound on the pieces of one (request, KV head) segment
   float scale;
   float scale_log2;
   unsigned* flags;             // device flag word (DEVFLAG_*)
@@ -60,10 +62,16 @@ struct DecodeParams {
   int withhold_copy;           // test hook: the producer skips its first copy
 };
 
-#ifndef GBATTN_DEC_CHUNK
-#define GBATTN_DEC_CHUNK 512
-#endif
-constexpr int kDecodeChunk = GBATTN_DEC_CHUNK;  // logical tokens per split (fixed: results depend only on logical positions)
+// Shortest range of (request, KV head, block) triples one decode warp streams, in
+// tokens.  It bounds the pieces a request's segment is cut into, and so the
+// workspace: ceil(max_seq_len / 256) + 1 pieces per (request, query head).
+constexpr int kDecodeMinRange = 256;
+
+struct DecodeWorkspace {
+  size_t off_part_lse, off_seg_first, off_plan, bytes;  // byte offsets (part_o at 0), size
+};
+DecodeWorkspace decode_workspace_layout(int S, int Hq, int D, int max_seq_len);
+int decode_max_pieces(int max_seq_len);
 
 // Paged decode.  tmK/tmV are 2-D tiled maps over the pools viewed as
 // [num_pool_blocks * Hkv * block_size, D] bf16 with a 64 x 16 box, 128-byte swizzle.

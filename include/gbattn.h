@@ -104,9 +104,13 @@ int paged_attn_prefill(const void *q, const void *k_pool, const void *v_pool,
                        float *lse, void *stream);
 
 /*
- * Bytes of scratch workspace paged_attn_decode needs for these sizes (partial
- * outputs of the split-KV pass).  Depends only on the arguments; the block size
- * is not one of them (it is fixed at 16 and checked by paged_attn_decode).
+ * Bytes of scratch workspace paged_attn_decode needs for these sizes.  The
+ * decode cuts the batch's (request, KV head, 16-token block) sequence into equal
+ * ranges of at least 256 tokens; each range that meets a request's cache yields
+ * one partial output (D fp32) and LSE per query head, at most
+ * ceil(max_seq_len / 256) + 1 per (request, query head).  Depends only on the
+ * arguments; the block size is not one of them (it is fixed at 16 and checked by
+ * paged_attn_decode).
  */
 size_t paged_attn_decode_workspace_size(int num_seqs, int Hq, int D, int max_seq_len);
 
@@ -128,7 +132,9 @@ size_t paged_attn_decode_workspace_size(int num_seqs, int Hq, int D, int max_seq
  *
  * The query of request r attends to all seq_lens[r] cached tokens.  A request
  * with seq_lens[r] == 0 gets O = 0 and LSE = -inf.  max_seq_len bounds every
- * seq_lens[r] (it sizes the split-KV grid).  block_size must be 16, D 64 or 128,
+ * seq_lens[r] (it sizes the workspace).  The split of the work depends on the
+ * lengths of the whole batch, never on where the blocks sit in the pool: the
+ * same inputs give the same bits, whatever the placement.  block_size must be 16, D 64 or 128,
  * Hq / Hkv <= 16.  Per-request data is checked on the device: a length outside
  * [0, min(max_seq_len, max_blocks_per_seq * block_size)] or a block id outside
  * [0, num_pool_blocks) makes that request's O and LSE NaN and sets a flag that
@@ -161,8 +167,8 @@ int paged_attn_decode(const void *q, const void *k_pool, const void *v_pool,
  *   - Sizes whose scratch, paged_attn_decode_workspace_size(num_seqs, Hq, D,
  *     max_seq_len), exceeds the array return ATTN_ERR_UNSUPPORTED before any
  *     work is enqueued (at D = 128 that is about 32,000 (request, query head,
- *     512-token chunk) partial results; 64 requests x 12 heads x 8192 tokens
- *     need 6.3 MB).
+ *     range) partial results; 64 requests x 12 heads x 8192 tokens need
+ *     13.1 MB).
  *   - The first call on a device looks up the array's device address (once,
  *     with that device current); make that first call before any stream
  *     capture begins.

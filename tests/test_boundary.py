@@ -113,11 +113,15 @@ def test_paged_decode_validation(lib, kw, code):
 
 
 def test_workspace_size_formula(lib):
+    # Per (request, query head): at most ceil(max_seq_len / 256) + 1 pieces (ranges
+    # of at least 16 blocks of 16 tokens), each D fp32 outputs and one fp32 LSE;
+    # then one int64 per (request, query head) for the segment starts and two
+    # int64 for the plan; every part 256-byte aligned.
+    up = lambda x: (x + 255) // 256 * 256
     for S, Hq, D, msl in [(64, 12, 128, 8192), (1, 1, 64, 1), (3, 8, 128, 513), (5, 4, 64, 0)]:
-        splits = max(1, math.ceil(msl / 512))
-        n = S * Hq * splits
-        part_o = (n * D * 4 + 255) // 256 * 256
-        expect = (part_o + n * 4 + 255) // 256 * 256
+        pieces = math.ceil(math.ceil(msl / 16) / 16) + 1
+        n = S * Hq * pieces
+        expect = up(n * D * 4) + up(n * 4) + up(S * Hq * 8) + up(16)
         assert lib.paged_attn_decode_workspace_size(S, Hq, D, msl) == expect
     assert lib.paged_attn_decode_workspace_size(-1, 1, 64, 1) == 0
 

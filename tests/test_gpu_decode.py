@@ -69,7 +69,7 @@ EDGE_LENS = [1, 2, 15, 16, 17, 31, 255, 511, 512, 513, 1024, 1500, 2048, 2049]
 
 
 @pytest.mark.parametrize("Hq,Hkv,D", [(12, 2, 128), (8, 8, 128), (16, 1, 64), (4, 2, 64),
-                                      (32, 2, 128), (6, 6, 64)])
+                                      (32, 2, 128), (6, 6, 64), (20, 2, 128), (9, 1, 64)])
 def test_decode_edge_lengths_and_groups(gb, Hq, Hkv, D):
     cfg = synth.DecodeConfig("edge", len(EDGE_LENS), Hq, Hkv, D, 1, 2049, 16,
                              13000 + Hq * 10 + D)
@@ -78,6 +78,19 @@ def test_decode_edge_lengths_and_groups(gb, Hq, Hkv, D):
     o_ref, lse_ref = oracle.paged_decode(p.q, p.k_pool, p.v_pool, p.block_table, p.seq_lens,
                                          cfg.softmax_scale)
     check_close(from_dev(o), from_dev(lse), o_ref, lse_ref, f"edge {Hq},{Hkv},{D}")
+
+
+def test_decode_long_requests_cut_into_many_pieces(gb):
+    """A batch of few, long requests: the work is cut into ranges of 16 blocks, so
+    the 16384-token request spans 65 pieces per head (two merge batches of 32) and
+    the others 36 and 1."""
+    lens = [16384, 9000, 1]
+    cfg = synth.DecodeConfig("pieces", len(lens), 12, 2, 128, 1, 16384, 16, 13050)
+    p = synth.paged_inputs(cfg, seq_lens=lens, max_seq_len=16384)
+    o, lse = run(gb, p, cfg.softmax_scale)
+    o_ref, lse_ref = oracle.paged_decode(p.q, p.k_pool, p.v_pool, p.block_table, p.seq_lens,
+                                         cfg.softmax_scale)
+    check_close(from_dev(o), from_dev(lse), o_ref, lse_ref, "many pieces")
 
 
 def test_decode_single_token_returns_v0_bit_exact(gb):
