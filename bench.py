@@ -551,7 +551,7 @@ def report_ours(args, res, world):
             "ms": {k: round(v, 5) for k, v in stats(res["t_dec"]).items()},
             "kv_bytes": res["kv_bytes"],
             "bytes_per_step": res["dec_bytes"],
-            "roofline": {"kernel": f"paged_decode_split_kernel<{DECODE.D}> + merge",
+            "roofline": {"kernel": f"paged_decode_split_kernel<{DECODE.D}, 1> + merge",
                          "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "peak_source": f"{src} copy bandwidth", "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4),
