@@ -304,10 +304,12 @@ struct MmaWarp {
   // tile occupies; the P V product reading them was issued earlier by this same
   // thread, and one thread's tcgen05.mma operations execute in issue order, so
   // that product has read P_I before this one writes there.
+  // Tile 1 uses the ring entries tile 0 has already waited for, whenever tile 0
+  // visits the same K/V tile (j < n0); then the phase is known to be complete.
   template <int I>
-  __device__ bool issue_s(int j) {
+  __device__ bool issue_s(int j, bool ring_seen) {
     const int ks = slot(2 * j);
-    if (!wait(bar.slot_full(ks), par(2 * j))) return false;
+    if (!ring_seen && !wait(bar.slot_full(ks), par(2 * j))) return false;
     tc_fence_after();
     const uint64_t a = dq + I * kTileStep, b = dk + static_cast<uint64_t>(ks) * kTileStep;
 #pragma unroll
@@ -323,9 +325,9 @@ struct MmaWarp {
 
   // O_I += P_I V_j (P_I from TMEM)
   template <int I>
-  __device__ bool issue_pv(int j, int nkv, int L) {
+  __device__ bool issue_pv(int j, int nkv, int L, bool ring_seen) {
     const int vs = slot(2 * j + 1);
-    if (!wait(bar.slot_full(vs), par(2 * j + 1))) return false;
+    if (!ring_seen && !wait(bar.slot_full(vs), par(2 * j + 1))) return false;
     if (PAGED && j == nkv - 1 && zeroed_j != j) {
       zeroed_j = j;
       // Key rows past the sequence end hold stale or arbitrary data (even NaN);
@@ -364,15 +366,15 @@ struct MmaWarp {
       s_left = n0 + n1;
       zeroed_j = -1;
       if (s_left == 0) mma_commit_warp(bar.q_empty());
-      if (n0 > 0 && !issue_s<0>(0)) return;
-      if (n1 > 0 && !issue_s<1>(0)) return;
+      if (n0 > 0 && !issue_s<0>(0, false)) return;
+      if (n1 > 0 && !issue_s<1>(0, n0 > 0)) return;
       if (nkv > 0) mma_commit_warp(bar.slot_empty(slot(0)));
       for (int j = 0; j < nkv; ++j) {
-        if (j < n0 && !issue_pv<0>(j, nkv, U.L)) return;
-        if (j + 1 < n0 && !issue_s<0>(j + 1)) return;
-        if (j < n1 && !issue_pv<1>(j, nkv, U.L)) return;
+        if (j < n0 && !issue_pv<0>(j, nkv, U.L, false)) return;
+        if (j + 1 < n0 && !issue_s<0>(j + 1, false)) return;
+        if (j < n1 && !issue_pv<1>(j, nkv, U.L, j < n0)) return;
         mma_commit_warp(bar.slot_empty(slot(2 * j + 1)));
-        if (j + 1 < n1 && !issue_s<1>(j + 1)) return;
+        if (j + 1 < n1 && !issue_s<1>(j + 1, j + 1 < n0)) return;
         if (j + 1 < nkv) mma_commit_warp(bar.slot_empty(slot(2 * j + 2)));
       }
       base += 2 * nkv;

@@ -316,6 +316,9 @@ __global__ void __launch_bounds__(kThreads, DecShape<NQT>::kCtasPerSm)
     };
     int phys = tt < n_w ? table_entry(c) : 0;
     int issued_end = 0;  // one past the last copy index issued
+    // every K/V byte is read once: let those lines go first, ahead of the
+    // partial results, queries and table entries that are read again
+    const uint64_t stream_policy = l2_policy_evict_first();
     bool stop = false;
     for (int t0 = 0; t0 < n_max && !stop; t0 += 8) {
       if (t0 + tt < n_w) {
@@ -349,9 +352,10 @@ __global__ void __launch_bounds__(kThreads, DecShape<NQT>::kCtasPerSm)
           mbar_arrive_expect_tx(bar_full + 8 * s, C::STAGE_BYTES);
 #pragma unroll
           for (int kb = 0; kb < C::KB; ++kb) {
-            tma_load_2d(dst + kb * C::BOX_BYTES, &tmK, bar_full + 8 * s, kb * 64, rows[l]);
-            tma_load_2d(dst + C::BLK_BYTES + kb * C::BOX_BYTES, &tmV, bar_full + 8 * s, kb * 64,
-                        rows[l]);
+            tma_load_2d_hint(dst + kb * C::BOX_BYTES, &tmK, bar_full + 8 * s, kb * 64, rows[l],
+                             stream_policy);
+            tma_load_2d_hint(dst + C::BLK_BYTES + kb * C::BOX_BYTES, &tmV, bar_full + 8 * s,
+                             kb * 64, rows[l], stream_policy);
           }
         }
       }
@@ -595,10 +599,10 @@ __global__ void __launch_bounds__(128)
       }
     }
   };
-  // Everything the first batch needs is requested at once: the length, the plan,
-  // the segment start and the LSE and partial outputs of the first 32 pieces (in
-  // bounds whatever the piece count turns out to be), so a segment of up to 32
-  // pieces costs one memory round trip.
+  // First round trip: the length, the plan, the segment start and the LSEs of the
+  // first 32 pieces (one word per lane, in bounds whatever the piece count turns
+  // out to be).  Second: the partial outputs of exactly the pieces that exist,
+  // 32 per round trip (reading the unused slots too would double the bytes).
   const int L = p.seq_lens[r];
   const long long NB = p.plan[0];
   const int W = static_cast<int>(p.plan[1]);
@@ -606,7 +610,6 @@ __global__ void __launch_bounds__(128)
       p.seg_first[static_cast<size_t>(r) * p.Hkv + (warp_global % p.Hq) / p.group];
   const int n_first = min(kBatch, p.max_pieces);
   const float lse_first = lane < n_first ? pl[lane] : 0.f;
-  load_batch(0, n_first);
 
   uint16_t* orow = static_cast<uint16_t*>(p.o) + hq * D + lane * PER;
   const float qnan = __int_as_float(0x7fc00000);
@@ -645,7 +648,7 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int i = 0; i < PER; ++i) res[i] = 0.f;
     for (int b0 = 0; b0 < ns; b0 += kBatch) {
-      if (b0 > 0) load_batch(b0, ns);
+      load_batch(b0, ns);
       const float lse_lane = b0 == 0 ? lse_first : (b0 + lane < ns ? pl[b0 + lane] : 0.f);
       const float w_lane = (b0 + lane < ns) ? __expf(lse_lane - M) : 0.f;
 #pragma unroll

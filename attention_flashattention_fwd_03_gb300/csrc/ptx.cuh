@@ -74,6 +74,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // try_wait that suspends the thread for at most hint_ns while the phase is
 // incomplete (it resumes as soon as the phase completes).
 __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
@@ -123,13 +136,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// The same wait for a whole warp: every lane polls, and the result (and the
-// abort / timeout decision, taken by lane 0) is the same in every lane, so the
-// warp stays converged for the .sync.aligned instructions that follow.
+// The same wait for a whole warp; the result (and the abort / timeout decision)
+// is the same in every lane, so the warp stays converged for the .sync.aligned
+// instructions that follow.  First lane 0 alone tests the phase without blocking:
+// most waits find it complete, and 32 lanes polling one mbarrier made even those
+// cost about 200 cycles.  (A lone lane blocking in try_wait with a suspend hint
+// while the rest of the warp waited at a shuffle was measured 5x slower overall:
+// the blocking poll stays warp-wide.)  The __syncwarp that follows (a barrier with memory ordering) orders
+// the other lanes' reads of the copied data after lane 0's observation, and lanes
+// that go on to tcgen05 work order it with tcgen05.fence::after_thread_sync.
+// Otherwise every lane polls until the phase completes.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
                                                unsigned* flags, unsigned long long limit_ns) {
   const uint32_t hint = poll_hint(limit_ns);
-  if (__all_sync(0xffffffffu, mbar_try_wait_hint(bar, parity, hint))) return true;
+  // common case: the phase has completed; one lane tests it without blocking
+  uint32_t ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_test_wait(bar, parity) ? 1u : 0u;
+  if (__shfl_sync(0xffffffffu, ok, 0)) {
+    __syncwarp();
+    return true;
+  }
+  // waiting: every lane polls (each lane then has observed the phase itself)
   const unsigned long long t0 = globaltimer();
   for (;;) {
     if (GBATTN_POLL_SLEEP_NS > 0) __nanosleep(GBATTN_POLL_SLEEP_NS);
@@ -179,6 +206,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// An L2 policy that marks lines as first to evict (for data read exactly once).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// tma_load_2d with an L2 cache policy for the fetched lines.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int c0, int c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
 
