@@ -207,13 +207,22 @@ __device__ void producer_warp(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     }
     ++uc;
     const int nblk_total = (U.L + kBS - 1) / kBS;
+    // paged: lane l < 8 reads the table entry of block l of a K/V tile; the next
+    // tile's entries are requested before this tile's copies are issued, so the
+    // table read is off the copy warp's path
+    auto table_entry = [&](int jj) -> int {
+      const int nb = min(BN / kBS, nblk_total - jj * (BN / kBS));
+      return lane < nb ? p.block_table[static_cast<size_t>(U.b) * p.max_blocks + jj * (BN / kBS) + lane]
+                       : 0;
+    };
+    int next_phys = (PAGED && U.nkv > 0) ? table_entry(0) : 0;
     for (int j = 0; j < U.nkv && ok; ++j) {
-      // paged: lanes 0..7 translate the tile's (up to) 8 blocks through the table
       int row_of_lane = 0, nblk = 0;
       if (PAGED) {
         nblk = min(BN / kBS, nblk_total - j * (BN / kBS));
+        int phys = next_phys;
+        if (j + 1 < U.nkv) next_phys = table_entry(j + 1);
         if (lane < nblk) {
-          int phys = p.block_table[static_cast<size_t>(U.b) * p.max_blocks + j * (BN / kBS) + lane];
           if (phys < 0 || phys >= p.num_pool_blocks) {
             raise_flag(p.flags, DEVFLAG_BAD_BLOCK);
             phys = 0;
@@ -238,16 +247,17 @@ __device__ void producer_warp(const CUtensorMap* tmQ, const CUtensorMap* tmK,
               tma_load_3d(dst + kb * C::BOX_BYTES, map, bar.slot_full(s), kb * 64, j * BN, U.bkv);
           }
         } else {
+          // lane 0 posts the byte count first; then lanes 0..nblk-1 copy their
+          // block's 16 rows, one box per 64-column half
           if (lane == 0) mbar_arrive_expect_tx(bar.slot_full(s), nblk * kBS * D * 2);
-          for (int blk = 0; blk < nblk; ++blk) {
-            const int row = __shfl_sync(0xffffffffu, row_of_lane, blk);
-            if (lane == 0) {
+          __syncwarp();
+          if (lane < nblk) {
 #pragma unroll
-              for (int kb = 0; kb < C::KB; ++kb)
-                tma_load_2d(dst + kb * C::BOX_BYTES + blk * kBS * 128, map, bar.slot_full(s),
-                            kb * 64, row);
-            }
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_2d(dst + kb * C::BOX_BYTES + lane * kBS * 128, map, bar.slot_full(s),
+                          kb * 64, row_of_lane);
           }
+          __syncwarp();
         }
         ++rc;
       }
