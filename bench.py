@@ -111,7 +111,10 @@ def stats(ms):
 # clocks sampled during the timed region
 # --------------------------------------------------------------------------- #
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 20 ms, each with its timestamp; stop() reports the
+    samples that fall inside the timed region (mark_region), or all samples when
+    none does (a region shorter than the sampling interval)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -120,12 +123,16 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.region = None
+
+    def mark_region(self, t0: float, t1: float):
+        self.region = (t0, t1)
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -147,26 +154,33 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
-            except ValueError:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]),
+                             [nm for nm, val in zip(names, parts[6:10]) if val.lower() == "active"]))
+            except (ValueError, IndexError):
                 continue
-            for nm, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "power_w_max": max(power) if power else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = rows
+        where = "all samples (none fell inside the timed region)"
+        if self.region is not None:
+            t0, t1 = self.region
+            sel = [r for r in rows if t0 - 0.02 <= r[0] <= t1 + 0.02]
+            if sel:
+                inside, where = sel, "samples inside the timed region"
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "power_w_max": max(r[3] for r in inside),
+                "reasons": sorted({nm for r in inside for nm in r[4]}),
+                "samples": len(inside), "samples_total": len(rows), "which": where}
 
 
 # --------------------------------------------------------------------------- #
@@ -343,8 +357,11 @@ def run_ours(args, rank, world, local_rank):
         sampler.start()
         time.sleep(0.3)
     wall0 = time.perf_counter()
+    region0 = time.time()
     t_pre, t_dec = R.time_calls([pre_call, dec_call], args.steps, 0)
     wall = time.perf_counter() - wall0
+    if sampler:
+        sampler.mark_region(region0, time.time())
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
