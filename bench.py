@@ -367,6 +367,10 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop() if sampler else None
     R.check_status("after timing")
 
+    # ---- the decode on its own (decode after decode, as in a serving loop) ----
+    (t_dec_alone,) = R.time_calls([dec_call], args.steps, max(args.warmup, 3))
+    R.check_status("after the decode loop")
+
     # ---- the other prefill workloads, each timed on its own ----
     other = {}
     for cfg in OTHER_PREFILL:
@@ -470,9 +474,9 @@ def run_ours(args, rank, world, local_rank):
     d2h = ho.numel() * 2 + hl.numel() * 4
 
     # ---- aggregate over ranks (max of medians) ----
-    names = ["pre", "dec", "e2e", "chunk", "naive"] + list(other)
+    names = ["pre", "dec", "e2e", "chunk", "naive", "dec_alone"] + list(other)
     meds = [stats(t_pre)["median"], stats(t_dec)["median"], stats(t_e2e)["median"],
-            stats(t_chunk)["median"], stats(t_naive)["median"]] + \
+            stats(t_chunk)["median"], stats(t_naive)["median"], stats(t_dec_alone)["median"]] + \
         [stats(other[n])["median"] for n in other]
     meds_max = max_over_ranks(meds + [wall], dev)
     med = dict(zip(names, meds_max[:-1]))
@@ -488,7 +492,8 @@ def run_ours(args, rank, world, local_rank):
                           f"in {info['seconds']:.1f} s"),
                "paged_decode": {"value": gbs, "unit": "GB/s", "cores": dcores, "kind": "oracle",
                                 "sample": f"the whole paged decode workload in {dsec:.2f} s"}}
-    return dict(med=med, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e, other=other,
+    return dict(med=med, t_pre=t_pre, t_dec=t_dec, t_dec_alone=t_dec_alone, t_e2e=t_e2e,
+                other=other,
                 t_chunk=t_chunk, chunk_flops=chunk_flops, us_eager=us_eager, us_graph=us_graph,
                 t_naive=t_naive,
                 wall=meds_max[-1], clocks=clocks, launches=args.steps * 3,
@@ -573,6 +578,15 @@ def report_ours(args, res, world):
                          "peak_source": f"{src} copy bandwidth", "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "traffic": load_traffic(f"paged_decode {DECODE.name}")},
+            "timed": "inside the headline step, right after the 1.4 ms prefill",
+            "alone": {
+                "what": "the same call timed in its own loop (decode after decode, as in a "
+                        "serving loop), L2 flushed the same way",
+                "value": round(res["dec_bytes"] / (med["dec_alone"] * 1e-3) / 1e9, 1),
+                "unit": "GB/s",
+                "ms": {k: round(v, 5) for k, v in stats(res["t_dec_alone"]).items()},
+                "frac": round(res["dec_bytes"] / (med["dec_alone"] * 1e-3) / 1e9
+                              / peaks["hbm_gbs"], 4)},
         },
         "paged_prefill": {
             "workload": (f"chunked prefill: {CHUNKED.num_seqs} sequences x {CHUNK_TQ} new tokens, "
