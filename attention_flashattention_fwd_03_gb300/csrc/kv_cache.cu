@@ -29,6 +29,9 @@ namespace {
 template <int D>
 __global__ void __launch_bounds__(256)
     paged_kv_append_kernel(const AppendParams p) {
+  // a decode launched next as a programmatic dependent may start its set-up now;
+  // it waits for this grid's writes before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long total = static_cast<long long>(p.S) * p.Hkv * p.Tn;

@@ -233,6 +233,10 @@ __global__ void __launch_bounds__(kThreads, DecShape<NQT>::kCtasPerSm)
     fence_barrier_init();
     fence_proxy_async_smem();
   }
+  // Launched as a programmatic dependent of whatever precedes it on the stream
+  // (the KV append of a decode step triggers early): everything up to here
+  // overlaps that kernel; its writes are complete and visible past this point.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == kConsumerWarps) {
     // ---------------- plan: total blocks, range count, this CTA's four ranges ----------------
@@ -730,22 +734,30 @@ cudaError_t launch_pair(const CUtensorMap& tmK, const CUtensorMap& tmV, const De
   auto grid_for = [&](int ctas_per_sm) {
     return static_cast<int>(max(1ll, min(static_cast<long long>(num_sms) * ctas_per_sm, want)));
   };
-  if (p.group <= 8)
-    paged_decode_split_kernel<D, 1><<<grid_for(DecShape<1>::kCtasPerSm), kThreads,
-                                      split_smem_bytes<D, 1>(), stream>>>(tmK, tmV, p);
-  else
-    paged_decode_split_kernel<D, 2><<<grid_for(DecShape<2>::kCtasPerSm), kThreads,
-                                      split_smem_bytes<D, 2>(), stream>>>(tmK, tmV, p);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t split = {};
+  split.blockDim = dim3(kThreads);
+  split.stream = stream;
+  split.attrs = attr;
+  split.numAttrs = 1;
+  cudaError_t e;
+  if (p.group <= 8) {
+    split.gridDim = dim3(grid_for(DecShape<1>::kCtasPerSm));
+    split.dynamicSmemBytes = split_smem_bytes<D, 1>();
+    e = cudaLaunchKernelEx(&split, paged_decode_split_kernel<D, 1>, tmK, tmV, p);
+  } else {
+    split.gridDim = dim3(grid_for(DecShape<2>::kCtasPerSm));
+    split.dynamicSmemBytes = split_smem_bytes<D, 2>();
+    e = cudaLaunchKernelEx(&split, paged_decode_split_kernel<D, 2>, tmK, tmV, p);
+  }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.S * p.Hq + 3) / 4);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel<D>, p);
