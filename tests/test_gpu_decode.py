@@ -93,6 +93,21 @@ def test_decode_long_requests_cut_into_many_pieces(gb):
     check_close(from_dev(o), from_dev(lse), o_ref, lse_ref, "many pieces")
 
 
+def test_decode_many_short_requests(gb):
+    """300 requests of 0..40 tokens: each warp's range crosses many one- to
+    three-block segments and skips the empty requests between them."""
+    rng = np.random.default_rng(13070)
+    lens = rng.choice([0, 1, 2, 15, 16, 17, 31, 33, 40], size=300).astype(np.int32)
+    cfg = synth.DecodeConfig("short", len(lens), 8, 2, 64, 0, 40, 16, 13070)
+    p = synth.paged_inputs(cfg, seq_lens=lens, max_seq_len=48)
+    o, lse = run(gb, p, cfg.softmax_scale)
+    o_ref, lse_ref = oracle.paged_decode(p.q, p.k_pool, p.v_pool, p.block_table, p.seq_lens,
+                                         cfg.softmax_scale)
+    live = p.seq_lens > 0
+    check_close(from_dev(o)[live], from_dev(lse)[live], o_ref[live], lse_ref[live], "short")
+    assert np.all(from_dev(o)[~live] == 0) and np.all(np.isneginf(from_dev(lse)[~live]))
+
+
 def test_decode_single_token_returns_v0_bit_exact(gb):
     cfg = synth.DecodeConfig("one", 3, 12, 2, 128, 1, 1, 16, 13100)
     p = synth.paged_inputs(cfg, seq_lens=[1, 1, 1], max_seq_len=16)
