@@ -14,9 +14,11 @@
 // 128-row query tiles of one (batch, head) that share every K/V tile:
 //   warp 0        producer: TMA loads of the unit's two Q tiles, then K_j, V_j
 //                 into one ring of 128-key slots (128-byte swizzle); in paged
-//                 mode the warp reads the tile's block-table entries and issues
-//                 one 16-row copy per block
-//   warp 1        MMA warp (one lane issues): S_i = Q_i K_j^T into TMEM (fp32),
+//                 mode lanes 0-7 read the tile's block-table entries (the next
+//                 tile's while this one is copied) and each copies its block's
+//                 16 rows
+//   warp 1        MMA warp (the converged warp runs the issue code; elect.sync
+//                 picks the lane that issues): S_i = Q_i K_j^T into TMEM (fp32),
 //                 then O_i += P_i V_j with P_i read from TMEM (tcgen05 A operand
 //                 in tensor memory), in the order P_0 V_j, S_0(j+1), P_1 V_j,
 //                 S_1(j+1); completion is signalled through tcgen05.commit on
