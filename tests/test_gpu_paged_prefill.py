@@ -66,6 +66,24 @@ def test_paged_prefill_matches_oracle(gb, Hq, Hkv, D, Tq, kv_lens, causal):
     check_against_oracle(o, lse, q, p, causal, cfg.softmax_scale, f"{Hq},{Hkv},{D},{Tq},{causal}")
 
 
+def test_paged_prefill_chunked_workload_full_size(gb):
+    """The chunked-prefill workload at its full size, every element against the
+    oracle: 16 sequences x 512 new tokens, cache lengths U[1024, 8192] with the
+    chunk included, GQA 32/8, D = 128, causal, 16-token blocks in a permuted pool."""
+    cfg = synth.DecodeConfig("chunked_prefill", 16, 32, 8, 128, 1024, 8192, 16, 6000)
+    p = synth.paged_inputs(cfg)
+    q = synth.normal_bf16(cfg.seed + 9, (cfg.num_seqs, cfg.Hq, 512, cfg.D))
+    o, lse = run(gb, q, p, True, cfg.softmax_scale)
+    o_ref, lse_ref = oracle.paged_prefill(q, p.k_pool, p.v_pool, p.block_table, p.seq_lens,
+                                          True, cfg.softmax_scale)
+    og, lg = from_dev(o), from_dev(lse)
+    err = np.abs(og - o_ref)
+    print(f"PARITY chunked_prefill rows={og.shape[0] * og.shape[1] * og.shape[2]} "
+          f"o_max_abs={err.max():.3e} o_mean_abs={err.mean():.3e} "
+          f"lse_max_abs={np.abs(lg - lse_ref).max():.3e}")
+    check_close(og, lg, o_ref, lse_ref, "chunked prefill, full size")
+
+
 def test_paged_prefill_short_cache_rows_see_nothing(gb):
     """kv_lens < Tq with a causal mask: the earliest queries see no key."""
     cfg = synth.DecodeConfig("short", 3, 4, 2, 128, 1, 300, 16, 21500)
